@@ -1,0 +1,493 @@
+#!/usr/bin/env python3
+"""Bench of paged-KV decode attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 1..5]
+
+One step is one pass of the decode hot path over one batch of the seeded
+synthetic workload (default: the Llama-3-8B-shaped GQA decode, 256 sequences,
+32 q / 8 kv heads, D=128, block 16, L~U[1024,8192], 4.8 GB of KV -- larger than
+L2, so no flush is needed between steps).  Rank 0 prints one JSON line with
+the whole-job HBM GB/s (algorithmic bytes: valid K/V + q + fp32 out + table
+entries + lengths), the roofline of the dominant kernel, an end-to-end figure
+through the public API with host buffers, the CPU oracle as a reference
+baseline, the SM clocks seen during the timed region, and the other named
+workloads measured the same way.
+
+With torchrun (N > 1) every rank runs its own replica of the batch (weak
+scaling, no collective on the data path); timing is bracketed by barriers and
+the slowest rank counts.  --impl reference times the CPU oracle instead (rank 0
+only) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "paged decode attention achieved HBM GB/s (% of 8 TB/s) and seq-steps/s, 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+DECODE_SOURCES = ["paged_kv_decode_pf_gb300/csrc/pf_decode.cuh", "paged_kv_decode_pf_gb300/csrc/pf_device.cuh",
+                  "paged_kv_decode_pf_gb300/csrc/pf_decode_d128.cu", "paged_kv_decode_pf_gb300/csrc/pf_decode_d64.cu"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-extras", action="store_true", help="skip the other named workloads")
+    ap.add_argument("--oracle-seconds", type=float, default=15.0, help="CPU work of the oracle baseline sample")
+    ap.add_argument("--decode-variant", default="decode", choices=["decode", "split"],
+                    help="headline path: single-pass decode or partition+merge")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch recorded by an ncu capture of the current decode sources, if any."""
+    sha = decode_source_sha()
+    pat = re.compile(r"traffic-record:\s+workload=(\S+)\s+kernel=(\S+)\s+bytes_per_launch=(\d+)\s+source_sha=(\w+)")
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            for m in pat.finditer(f.read()):
+                if m.group(1) == workload and m.group(4) == sha:
+                    return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (100 ms) of SM clock and throttle reasons around the timed region."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.t_start = self.t_end = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_id}", "--query-gpu=" + ",".join(self.FIELDS),
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def start(self):
+        self.t_start = time.time()
+
+    def stop(self):
+        self.t_end = time.time()
+
+    def close(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        win = [p for t, p in self.samples if self.t_start is not None and self.t_start <= t <= (self.t_end or t)]
+        src = "timed region"
+        if not win:
+            win = [p for _, p in self.samples]
+            src = "whole run (timed region shorter than the sampling period)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in win if num(p[0]) is not None]
+        smax = [num(p[1]) for p in win if num(p[1]) is not None]
+        pw = [num(p[2]) for p in win if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in win for n, v in zip(names, p[4:]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(win), "window": src}
+
+
+# -------------------------------------------------------------- GPU runner
+
+class Runner:
+    """Device-resident inputs of one workload and the launches of one step."""
+
+    def __init__(self, pf, wl, dev, variant="decode"):
+        import torch
+        self.pf, self.wl, self.dev = pf, wl, dev
+
+        def bf(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        self.q, self.kc, self.vc = bf(wl.q), bf(wl.k_cache), bf(wl.v_cache)
+        self.bt = torch.from_numpy(wl.block_tables).to(dev)
+        self.cl = torch.from_numpy(wl.context_lens).to(dev)
+        self.out = torch.empty((wl.num_seqs, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
+        self.append = wl.slot_mapping is not None
+        if self.append:
+            self.nk, self.nv = bf(wl.new_k), bf(wl.new_v)
+            self.sm = torch.from_numpy(wl.slot_mapping).to(dev)
+        self.split = variant == "split" or wl.partition_size is not None
+        if self.split:
+            self.P = wl.partition_size or 512
+            self.max_ctx = wl.max_context_len
+            self.ws = pf.alloc_workspace(wl.num_seqs, wl.num_q_heads, wl.head_dim, self.max_ctx, self.P, dev)
+        self.kernels_per_step = (1 if self.append else 0) + (2 if self.split else 1)
+        self.dominant = "partition" if self.split else "decode"
+
+    def step(self, ev=None):
+        """One pass; when `ev` is a pair of CUDA events they bracket the dominant kernel."""
+        pf = self.pf
+        if self.append:
+            pf.reshape_and_cache(self.nk, self.nv, self.sm, self.kc, self.vc)
+        if ev is not None:
+            ev[0].record()
+        if self.split:
+            pf.paged_attention_decode_partition(self.q, self.kc, self.vc, self.bt, self.cl, self.P, self.max_ctx,
+                                                self.ws, self.wl.scale)
+            if ev is not None:
+                ev[1].record()
+            pf.paged_attention_merge(self.ws, self.cl, self.wl.num_q_heads, self.wl.head_dim, self.P, self.max_ctx,
+                                     self.out)
+        else:
+            pf.paged_attention_decode(self.q, self.kc, self.vc, self.bt, self.cl, self.wl.scale, self.out)
+            if ev is not None:
+                ev[1].record()
+
+    def step_bytes(self):
+        return self.wl.algorithmic_bytes(with_append=self.append)
+
+    def dominant_bytes(self):
+        """Algorithmic bytes of the dominant kernel alone."""
+        wl = self.wl
+        b = wl.algorithmic_bytes(with_append=False)
+        if self.split:     # the partition pass reads everything but writes partials, not out
+            b -= wl.num_seqs * wl.num_q_heads * wl.head_dim * 4
+        return b
+
+
+def time_steps(runner, steps, warmup, flush=None, dist=None, sampler=None):
+    """(ms per step over the timed region, mean ms of the dominant kernel, per-launch ms list)."""
+    import torch
+    for _ in range(warmup):
+        runner.step()
+        if flush is not None:
+            flush.zero_()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    if sampler is not None:
+        sampler.start()
+    t0.record()
+    for k in range(steps):
+        runner.step(evs[k])
+        if flush is not None:
+            flush.zero_()
+    t1.record()
+    torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.stop()
+    if dist is not None:
+        dist.barrier()
+    total = t0.elapsed_time(t1)
+    per = [a.elapsed_time(b) for a, b in evs]
+    return total / steps, statistics.fmean(per), per
+
+
+def time_e2e(runner, steps, warmup):
+    """Same step through the public API with the per-step inputs copied from pinned host memory
+    and the output read back; the KV cache is the resident state the step reads in place."""
+    import torch
+    wl = runner.wl
+    host_in = [(runner.q, torch.from_numpy(wl.q.view(np.int16)).view(torch.bfloat16).pin_memory()),
+               (runner.bt, torch.from_numpy(wl.block_tables).pin_memory()),
+               (runner.cl, torch.from_numpy(wl.context_lens).pin_memory())]
+    if runner.append:
+        host_in += [(runner.nk, torch.from_numpy(wl.new_k.view(np.int16)).view(torch.bfloat16).pin_memory()),
+                    (runner.nv, torch.from_numpy(wl.new_v.view(np.int16)).view(torch.bfloat16).pin_memory()),
+                    (runner.sm, torch.from_numpy(wl.slot_mapping).pin_memory())]
+    out_host = torch.empty(runner.out.shape, dtype=runner.out.dtype).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for _, h in host_in)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for d, h in host_in:
+            d.copy_(h, non_blocking=True)
+        runner.step()
+        out_host.copy_(runner.out, non_blocking=True)
+    for _ in range(warmup):
+        one()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record()
+    for _ in range(steps):
+        one()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps, h2d, d2h
+
+
+def workload_description(wl, index):
+    from workloads import CONFIGS
+    return f"{CONFIGS[index].name}: {CONFIGS[index].description} (seed {wl.seed})"
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample_run(orc, wl, target_s, threads=0):
+    """Time the oracle on the first n sequences, n calibrated to about target_s seconds.
+    Returns (seconds, sample bytes, n, description)."""
+    import dataclasses
+
+    def sub(n):
+        return dataclasses.replace(wl, num_seqs=n, q=wl.q[:n], block_tables=wl.block_tables[:n],
+                                   context_lens=wl.context_lens[:n], slot_mapping=None, new_k=None, new_v=None)
+
+    def run(w):
+        t = time.perf_counter()
+        orc.paged_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, threads=threads)
+        return time.perf_counter() - t
+    t1 = run(sub(1))
+    n = int(max(1, min(wl.num_seqs, math.floor(target_s / max(t1, 1e-6)))))
+    w = sub(n)
+    secs = run(w) if n > 1 else t1
+    tokens = int(w.context_lens.astype(np.int64).sum())
+    desc = f"first {n} of {wl.num_seqs} sequences, all {wl.num_q_heads} query heads ({tokens} tokens)"
+    return secs, w.algorithmic_bytes(), n, desc
+
+
+# ------------------------------------------------------------------- main
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    peak, peak_src = measured_peak()
+
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import torch
+    import torch.distributed as tdist
+
+    dist = None
+    if world > 1:
+        tdist.init_process_group(backend="nccl", init_method="env://")
+        dist = tdist
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+
+    from paged_kv_decode_pf_gb300 import _build
+    if rank == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    import paged_kv_decode_pf_gb300 as pf
+    from workloads import CONFIGS, make_config
+
+    wl = make_config(args.workload)
+    runner = Runner(pf, wl, dev, args.decode_variant)
+    flush = None
+    if runner.step_bytes() < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local_rank)
+    sampler = ClockSampler(gpu_id)
+    ms_step, ms_dom, per = time_steps(runner, args.steps, max(args.warmup, 3), flush, dist, sampler)
+    pf.check_device_error()
+    sampler.close()
+    if dist is not None:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    step_bytes = runner.step_bytes()
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    dom_bytes = runner.dominant_bytes()
+    achieved = dom_bytes / (ms_dom * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = time_e2e(runner, min(args.steps, 500), 3)
+    pf.check_device_error()
+    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+
+    extras = {}
+    if not args.no_extras and rank == 0:
+        del runner
+        torch.cuda.empty_cache()
+        for idx in [1, 2, 3, 5]:
+            if idx == args.workload:
+                continue
+            w = make_config(idx)
+            r = Runner(pf, w, dev)
+            fl = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if r.step_bytes() < 2 * L2_BYTES \
+                else None
+            n = 200 if fl is None else 400
+            ms_s, ms_d, _ = time_steps(r, n, 10, fl)
+            pf.check_device_error()
+            b = r.step_bytes()
+            extras[CONFIGS[idx].name] = {
+                "description": CONFIGS[idx].description,
+                "step": ("append + " if r.append else "") + ("partition + merge" if r.split else "decode"),
+                "us_per_step": round(ms_s * 1e3, 2) if fl is None else None,
+                "us_dominant_kernel": round(ms_d * 1e3, 2),
+                "algorithmic_bytes": b,
+                "gbs_step": round(b / (ms_s * 1e-3) / 1e9, 1) if fl is None else None,
+                "gbs_dominant_kernel": round(r.dominant_bytes() / (ms_d * 1e-3) / 1e9, 1),
+                "pct_of_8tbs_dominant": round(100 * r.dominant_bytes() / (ms_d * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
+                "seq_steps_per_s": round(w.num_seqs / ((ms_s if fl is None else ms_d) * 1e-3), 1),
+                "l2": "flushed between steps (kernel time only)" if fl is not None else "inputs larger than L2",
+            }
+            del r, fl
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0:
+        import oracle
+        orc = oracle.load()
+        secs, sb, n, desc = oracle_sample_run(orc, wl, args.oracle_seconds)
+        cpu = {"value": round(sb / secs / 1e9, 4), "unit": "GB/s", "cores": orc.max_threads(), "kind": "oracle",
+               "sample": desc, "seconds": round(secs, 3),
+               "seq_steps_per_s": round(n / secs, 3)}
+
+    if rank == 0:
+        clocks = sampler.summary()
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "storage_dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_description(wl, args.workload), "num_seqs": wl.num_seqs,
+                       "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                       "block_size": wl.block_size, "total_tokens": int(wl.context_lens.astype(np.int64).sum()),
+                       "step": "pf_paged_attention_decode" if not runner_split(args, wl) else
+                       "pf_paged_attention_decode_partition + pf_paged_attention_merge",
+                       "algorithmic_bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2, no flush" if flush is None else "L2 flushed between steps",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "seq_steps_per_s": round(world * wl.num_seqs / (ms_step * 1e-3), 1),
+            "us_per_call": round(ms_step * 1e3, 2),
+            "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic(CONFIGS[args.workload].name),
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                         else "fallback 6.8 TB/s", "kernel": runner_kernel(args, wl),
+                         "kernel_us_mean": round(ms_dom * 1e3, 2),
+                         "kernel_us_p10_p90": [round(float(np.percentile(per, 10)) * 1e3, 2),
+                                               round(float(np.percentile(per, 90)) * 1e3, 2)]},
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_ms * 1e3, 2),
+                    "note": "per-step inputs (q, block tables, lengths) copied from pinned host memory and "
+                            "out read back each step; the KV cache stays resident"},
+            "gpu_launches": args.steps * kernels_per_step(args, wl),
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "workloads": extras,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def runner_split(args, wl):
+    return args.decode_variant == "split" or wl.partition_size is not None
+
+
+def runner_kernel(args, wl):
+    return "paged_decode_kernel (partition pass)" if runner_split(args, wl) else "paged_decode_kernel"
+
+
+def kernels_per_step(args, wl):
+    return (1 if wl.slot_mapping is not None else 0) + (2 if runner_split(args, wl) else 1)
+
+
+def reference_arm(args, rank, world):
+    """The CPU oracle as the reference arm: rank 0 times it on a bounded sample per step."""
+    if rank != 0:
+        return
+    import oracle
+    from workloads import make_config
+    wl = make_config(args.workload)
+    orc = oracle.load()
+    steps, warmup = args.steps, max(args.warmup, 3)
+    per_step = max(0.02, min(args.oracle_seconds, 150.0 / (steps + warmup)))
+    secs1, sb, n, desc = oracle_sample_run(orc, wl, per_step)
+    import dataclasses
+    w = dataclasses.replace(wl, num_seqs=n, q=wl.q[:n], block_tables=wl.block_tables[:n],
+                            context_lens=wl.context_lens[:n], slot_mapping=None, new_k=None, new_v=None)
+    for _ in range(warmup):
+        orc.paged_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale)
+    t = time.perf_counter()
+    for _ in range(steps):
+        orc.paged_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale)
+    el = (time.perf_counter() - t) / steps
+    value = round(sb / el / 1e9, 4)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": warmup, "ms_per_step": round(el * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_description(wl, args.workload), "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": orc.max_threads(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

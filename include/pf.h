@@ -1,0 +1,199 @@
+/*
+ * pf.h -- C ABI of libpf.so: paged-KV decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the decode step of a paged KV cache:
+ *   - "Physical KV blocks with logical per-request block tables" and
+ *     "Decode-only block-table attention reads physical KV blocks directly; the
+ *     Triton kernel uses online softmax without constructing padded batch-wide
+ *     K/V" (ForgeLLM README, feature list), with "grouped-query attention"
+ *     (same list, "Llama-family decoder");
+ *   - "Paged KV cache allocates fixed-size blocks on demand" (LLM-Inference-Engine
+ *     README, "Why paged KV cache?");
+ *   - "Decode is memory-bound" (same README, "Why dynamic injection during
+ *     decode?") -- every kernel here streams the cache once and is bounded by
+ *     HBM bandwidth.
+ *
+ * Conventions shared by every call
+ *   bf16       IEEE binary32 truncated to its upper 16 bits, stored as uint16.
+ *   Layouts    (all row-major, contiguous, no padding)
+ *              q             [num_seqs, num_q_heads, head_dim]          bf16
+ *              k, v          [num_tokens, num_kv_heads, head_dim]       bf16
+ *              k_cache,
+ *              v_cache       [num_blocks, num_kv_heads, block_size, head_dim] bf16
+ *              block_tables  [num_seqs, max_blocks_per_seq]             int32
+ *              context_lens  [num_seqs]                                 int32
+ *              out           [num_seqs, num_q_heads, head_dim]          fp32
+ *   Paging     token t of sequence i is stored in physical block
+ *              block_tables[i][t / block_size] at offset t % block_size.
+ *              Table entries at or past ceil(context_lens[i] / block_size) are
+ *              never read.
+ *   GQA        query head h reads kv head h / (num_q_heads / num_kv_heads)
+ *              (contiguous groups).
+ *   Memory     every pointer is device memory owned by the caller; nothing is
+ *              retained after a call returns.  q, k, v, the caches, out and the
+ *              workspace must be 16-byte aligned (workspace: 256-byte),
+ *              block_tables / context_lens 4-byte, slot_mapping 8-byte.
+ *   Streams    every call is asynchronous and stream-ordered on `stream`
+ *              (a cudaStream_t; NULL is the legacy default stream).  Calls are
+ *              thread-safe.  The current CUDA device must own all pointers.
+ *   Errors     problems visible on the host (null or misaligned pointers,
+ *              non-positive sizes, overflowing sizes) return PF_ERR_INVALID_ARG
+ *              and shapes outside the compiled set return PF_ERR_UNSUPPORTED,
+ *              both before anything is launched; a failed launch returns
+ *              PF_ERR_CUDA.  Problems only the device can see -- a slot or a
+ *              block id out of range, a context length the table or the
+ *              partition grid cannot hold, a bounded wait that gave up -- never
+ *              trap: the kernel skips the offending row (append) or writes NaN
+ *              to the affected output rows (attention), sets a bit in a
+ *              per-device error word, and pf_get_device_error() reports it.
+ */
+#ifndef PF_H
+#define PF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PF_API __attribute__((visibility("default")))
+#else
+#define PF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA header. */
+typedef struct CUstream_st* pf_stream_t;
+
+typedef enum pf_status {
+    PF_OK = 0,
+    PF_ERR_INVALID_ARG = 1,     /* host-visible argument error; nothing launched */
+    PF_ERR_UNSUPPORTED = 2,     /* valid but not compiled: head_dim, block_size or group */
+    PF_ERR_CUDA = 3,            /* a CUDA runtime call or launch failed */
+    PF_ERR_DEVICE_BOUNDS = 4,   /* device saw a slot / block id / length out of range */
+    PF_ERR_DEVICE_TIMEOUT = 5   /* a bounded device-side wait gave up */
+} pf_status;
+
+/*
+ * KV append ("reshape_and_cache"): writes each new token's K and V into its
+ * physical slot -- the write side of the ForgeLLM README's "Physical KV blocks
+ * with logical per-request block tables".
+ *
+ *   for every token i < num_tokens with s = slot_mapping[i] != -1, every kv head h:
+ *     k_cache[s / block_size][h][s % block_size][:] = k[i][h][:]
+ *     v_cache[s / block_size][h][s % block_size][:] = v[i][h][:]
+ *
+ * Bit-exact copy.  Slots equal to -1 are padding and are skipped.  Any other
+ * negative slot or a slot >= num_blocks * block_size is skipped and flags
+ * PF_ERR_DEVICE_BOUNDS.  Valid slots must be distinct within one call (the
+ * result is unspecified otherwise).  head_dim must be a multiple of 8;
+ * any block_size >= 1.  num_tokens == 0 launches nothing.
+ */
+PF_API pf_status pf_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping,
+                               void* k_cache, void* v_cache, int64_t num_tokens,
+                               int num_kv_heads, int head_dim, int block_size,
+                               int64_t num_blocks, pf_stream_t stream);
+
+/*
+ * Decode attention over the paged cache, one query token per sequence, in a
+ * single pass (ForgeLLM README, feature list: decode-only block-table attention
+ * with online softmax, grouped-query heads):
+ *
+ *   out[i][h][:] = sum_t softmax_t(scale * q[i][h] . K_t) V_t,   t < context_lens[i],
+ *   K_t, V_t = k_cache/v_cache[block_tables[i][t / bs]][h / g][t % bs][:]
+ *
+ * fp32 accumulation and an fp32 online softmax; out is fp32.
+ * context_lens[i] == 0 gives a zero row.  Supported: head_dim in {64, 128},
+ * block_size a multiple of 16 (the configurations use 16 and 32),
+ * g = num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ * A context length above max_blocks_per_seq * block_size, or a table entry
+ * outside [0, num_blocks), flags PF_ERR_DEVICE_BOUNDS and NaN-fills the rows
+ * of that (sequence, kv head).
+ */
+PF_API pf_status pf_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, const int32_t* context_lens,
+                                    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                    float scale, float* out, pf_stream_t stream);
+
+/*
+ * Split over context partitions ("flash-decoding") for long contexts.
+ *
+ * The workspace holds, for NP = ceil(max_context_len / partition_size)
+ * partitions, three fp32 arrays, each starting on a 256-byte boundary:
+ *   tmp_out [num_seqs][num_q_heads][NP][head_dim]  o_k = sum e_t V_t / l_k
+ *   tmp_m   [num_seqs][num_q_heads][NP]            m_k = max_t scale*q.K_t
+ *   tmp_l   [num_seqs][num_q_heads][NP]            l_k = sum_t exp(s_t - m_k)
+ * over the tokens [k*P, (k+1)*P) of each sequence.  Only the partitions
+ * k < ceil(context_lens[i] / P) are written.
+ *
+ * pf_paged_attention_partition_workspace_layout() returns the byte offsets of
+ * the three arrays and the total size (0 on invalid arguments); the size query
+ * returns just the total.  partition_size must be a positive multiple of 16
+ * (tiles of 16 tokens never straddle two partitions).
+ */
+PF_API size_t pf_paged_attention_partition_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
+                                                     int max_context_len, int partition_size,
+                                                     size_t* tmp_out_offset, size_t* tmp_m_offset,
+                                                     size_t* tmp_l_offset);
+PF_API size_t pf_paged_attention_partition_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                                   int max_context_len, int partition_size);
+
+/*
+ * Partition pass: the decode computation restricted to each context
+ * partition, writing (o_k, m_k, l_k) into the workspace.  Same arguments and
+ * supported shapes as pf_paged_attention_decode plus partition_size, the
+ * max_context_len the workspace was sized for (every context_lens[i] must be
+ * <= it; a longer one flags PF_ERR_DEVICE_BOUNDS and NaN-fills its partials),
+ * the workspace and its size in bytes (checked against the layout).
+ */
+PF_API pf_status pf_paged_attention_decode_partition(const void* q, const void* k_cache, const void* v_cache,
+                                              const int32_t* block_tables, const int32_t* context_lens,
+                                              int num_seqs, int num_q_heads, int num_kv_heads,
+                                              int head_dim, int block_size, int max_blocks_per_seq,
+                                              int64_t num_blocks, float scale, int partition_size,
+                                              int max_context_len, void* workspace,
+                                              size_t workspace_bytes, pf_stream_t stream);
+
+/*
+ * Log-sum-exp merge of the partitions written by the partition pass:
+ *   M = max_k m_k,  w_k = l_k exp(m_k - M),  out = sum_k w_k o_k / sum_k w_k
+ * over k < ceil(context_lens[i] / partition_size); zero rows for empty
+ * sequences.  The arguments must match the partition pass that filled the
+ * workspace.  head_dim in {64, 128}.
+ */
+PF_API pf_status pf_paged_attention_merge(const void* workspace, const int32_t* context_lens, int num_seqs,
+                                   int num_q_heads, int head_dim, int partition_size,
+                                   int max_context_len, float* out, pf_stream_t stream);
+
+/*
+ * Device error word of the current device.  Synchronises `stream`, reads the
+ * word, clears it and returns PF_ERR_DEVICE_TIMEOUT or PF_ERR_DEVICE_BOUNDS if
+ * the corresponding bit was set (timeout first), PF_ERR_CUDA if the
+ * synchronisation or the read failed, PF_OK otherwise.  The word collects the
+ * errors of every call on the device since it was last read.
+ */
+PF_API pf_status pf_get_device_error(pf_stream_t stream);
+
+/* Static, human-readable name of a status. */
+PF_API const char* pf_status_string(pf_status status);
+
+/*
+ * Failure-detection check (not part of the paper's method): launches one
+ * block whose thread waits on a shared-memory barrier that nothing completes,
+ * through the same bounded wait the attention kernels use, giving up after
+ * about limit_ns nanoseconds (1e3 .. 1e10).  The kernel then returns normally,
+ * with PF_ERR_DEVICE_TIMEOUT set in the error word.  It exists so that tests
+ * can exercise the timeout path without disturbing the GPU.
+ */
+PF_API pf_status pf_debug_bounded_wait(int64_t limit_ns, pf_stream_t stream);
+
+/* Library version, e.g. "0.1.0". */
+PF_API const char* pf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PF_H */

@@ -1,0 +1,421 @@
+// C ABI of libpf.so (declared in include/pf.h): argument validation, launch
+// configuration, the per-device error word, and the small kernels that are not
+// the decode loop itself -- the KV-append scatter, the log-sum-exp merge of
+// context partitions and the bounded-wait check.
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "pf.h"
+#include "pf_device.cuh"
+#include "pf_internal.h"
+
+namespace pf {
+
+// ------------------------------------------------------------- error word
+
+// One word per device (each context holds its own copy of this variable).
+__device__ unsigned int g_error_word;
+
+static std::atomic<unsigned*> g_error_ptr[64];
+static std::atomic<int> g_sm_count[64];
+
+static cudaError_t current_device(int* dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return e;
+    return (*dev >= 0 && *dev < 64) ? cudaSuccess : cudaErrorInvalidDevice;
+}
+
+// Device address of the error word of the current device, looked up once per device.
+static cudaError_t error_word(unsigned** out) {
+    int dev = 0;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return e;
+    unsigned* p = g_error_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_error_word);
+        if (e != cudaSuccess) return e;
+        g_error_ptr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return cudaSuccess;
+}
+
+static cudaError_t sm_count(int* out) {
+    int dev = 0;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return e;
+    int n = g_sm_count[dev].load(std::memory_order_acquire);
+    if (n <= 0) {
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_sm_count[dev].store(n, std::memory_order_release);
+    }
+    *out = n;
+    return cudaSuccess;
+}
+
+// ------------------------------------------------------------------ append
+
+// One thread per 16-byte chunk of a (token, kv head) row; copies the K and the V chunk.
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __restrict__ k,
+                                                                const uint4* __restrict__ v,
+                                                                const int64_t* __restrict__ slots,
+                                                                uint4* __restrict__ k_cache,
+                                                                uint4* __restrict__ v_cache, long long total,
+                                                                int num_kv_heads, int chunks_per_row,
+                                                                int block_size, long long num_slots,
+                                                                unsigned* err) {
+    const int row_chunks = num_kv_heads * chunks_per_row;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long i = idx / row_chunks;
+        const int rem = int(idx - i * row_chunks);
+        const long long s = __ldg(slots + i);
+        if (s == -1) continue;  // padding token
+        if (s < 0 || s >= num_slots) {
+            if (rem == 0) set_error(err, ERR_BOUNDS);
+            continue;
+        }
+        const int h = rem / chunks_per_row, c = rem - h * chunks_per_row;
+        const long long blk = s / block_size;
+        const int off = int(s - blk * block_size);
+        const long long dst = ((blk * num_kv_heads + h) * block_size + off) * chunks_per_row + c;
+        k_cache[dst] = __ldg(k + idx);
+        v_cache[dst] = __ldg(v + idx);
+    }
+}
+
+// ------------------------------------------------------------------- merge
+
+// One warp per (sequence, query head): log-sum-exp merge of its partitions.
+template <int D>
+__global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict__ tmp_out,
+                                                        const float* __restrict__ tmp_m,
+                                                        const float* __restrict__ tmp_l,
+                                                        const int32_t* __restrict__ context_lens, int num_seqs,
+                                                        int num_q_heads, int partition_size,
+                                                        int num_partitions, int max_context_len,
+                                                        float* __restrict__ out, unsigned* err) {
+    constexpr int DPL = D / 32;
+    constexpr float kLog2e = 1.4426950408889634f;
+    const long long gw = blockIdx.x * (long long)(blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= (long long)num_seqs * num_q_heads) return;
+    const int seq = int(gw / num_q_heads);
+    const int L = __ldg(context_lens + seq);
+    float* o = out + gw * D + lane * DPL;
+    if (L < 0 || L > max_context_len) {
+        if (lane == 0) set_error(err, ERR_BOUNDS);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[e] = NAN;
+        return;
+    }
+    const int np = (L + partition_size - 1) / partition_size;
+    const size_t base = size_t(gw) * num_partitions;
+    float acc[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+    if (np == 0) {
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[e] = 0.f;
+        return;
+    }
+    float M = -INFINITY;
+    for (int k = lane; k < np; k += 32) M = fmaxf(M, tmp_m[base + k]);
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, s));
+    float W = 0.f;
+    for (int k0 = 0; k0 < np; k0 += 32) {
+        const int k = k0 + lane;
+        const float wk = k < np ? tmp_l[base + k] * exp2_approx((tmp_m[base + k] - M) * kLog2e) : 0.f;
+        W += wk;
+        const int n = min(32, np - k0);
+        for (int j = 0; j < n; ++j) {
+            const float w = __shfl_sync(FULL_MASK, wk, j);
+            const float* src = tmp_out + (base + k0 + j) * D + lane * DPL;
+            if constexpr (DPL == 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src);
+                acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2*>(src);
+                acc[0] += w * x.x; acc[1] += w * x.y;
+            }
+        }
+    }
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) W += __shfl_xor_sync(FULL_MASK, W, s);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] = acc[e] / W;
+}
+
+// ------------------------------------------------------ bounded-wait check
+
+// Waits on a barrier that nothing completes, through the same bounded wait as
+// the attention kernels; there are no copies in flight, so giving up is clean.
+__global__ void bounded_wait_kernel(unsigned* err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait_bounded(b, 0, limit_ns)) set_error(err, ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ helpers
+
+static bool aligned(const void* p, size_t a) { return p != nullptr && reinterpret_cast<uintptr_t>(p) % a == 0; }
+static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+static int log2_int(int x) {
+    int s = 0;
+    while ((1 << s) < x) ++s;
+    return s;
+}
+
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// a * b * c * d without overflow of size_t, or SIZE_MAX
+static size_t mul_sat(size_t a, size_t b) { return (b != 0 && a > SIZE_MAX / b) ? SIZE_MAX : a * b; }
+
+struct AttnArgs {
+    const void* q; const void* k_cache; const void* v_cache;
+    const int32_t* block_tables; const int32_t* context_lens;
+    int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq;
+    int64_t num_blocks;
+    float scale;
+};
+
+static pf_status check_attention(const AttnArgs& a) {
+    if (a.num_seqs < 0 || a.num_q_heads <= 0 || a.num_kv_heads <= 0 || a.head_dim <= 0 || a.block_size <= 0 ||
+        a.max_blocks_per_seq <= 0 || a.num_blocks <= 0 || !std::isfinite(a.scale))
+        return PF_ERR_INVALID_ARG;
+    if (a.num_q_heads % a.num_kv_heads != 0) return PF_ERR_INVALID_ARG;
+    if (a.num_blocks > INT32_MAX) return PF_ERR_INVALID_ARG;  // table entries are int32
+    const size_t cache_elems =
+        mul_sat(mul_sat(mul_sat(size_t(a.num_blocks), size_t(a.num_kv_heads)), size_t(a.block_size)),
+                size_t(a.head_dim));
+    if (cache_elems >= (SIZE_MAX >> 2)) return PF_ERR_INVALID_ARG;
+    if ((long long)a.num_seqs * a.num_kv_heads > INT32_MAX) return PF_ERR_INVALID_ARG;
+    if (a.num_seqs > 0 && (!aligned(a.q, 16) || !aligned(a.k_cache, 16) || !aligned(a.v_cache, 16) ||
+                           !aligned(a.block_tables, 4) || !aligned(a.context_lens, 4)))
+        return PF_ERR_INVALID_ARG;
+    const int g = a.num_q_heads / a.num_kv_heads;
+    if (a.head_dim != 64 && a.head_dim != 128) return PF_ERR_UNSUPPORTED;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return PF_ERR_UNSUPPORTED;
+    if (a.block_size % kTileTokens != 0) return PF_ERR_UNSUPPORTED;
+    return PF_OK;
+}
+
+static DecodeParams make_params(const AttnArgs& a, unsigned* err) {
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(a.q);
+    p.k_cache = static_cast<const uint16_t*>(a.k_cache);
+    p.v_cache = static_cast<const uint16_t*>(a.v_cache);
+    p.block_tables = a.block_tables;
+    p.context_lens = a.context_lens;
+    p.err = err;
+    p.num_blocks = a.num_blocks;
+    p.wait_limit_ns = kDefaultWaitLimitNs;
+    p.scale_log2 = float(double(a.scale) * 1.4426950408889634);
+    p.num_seqs = a.num_seqs;
+    p.num_q_heads = a.num_q_heads;
+    p.num_kv_heads = a.num_kv_heads;
+    p.block_size = a.block_size;
+    p.block_shift = is_pow2(a.block_size) ? log2_int(a.block_size) : -1;
+    p.max_blocks_per_seq = a.max_blocks_per_seq;
+    return p;
+}
+
+static cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool partition,
+                                 cudaStream_t stream) {
+    return head_dim == 64 ? launch_decode_d64(p, group, partition, stream)
+                          : launch_decode_d128(p, group, partition, stream);
+}
+
+}  // namespace pf
+
+using namespace pf;
+
+// ======================================================================= ABI
+
+extern "C" {
+
+const char* pf_version(void) { return "0.1.0"; }
+
+const char* pf_status_string(pf_status s) {
+    switch (s) {
+        case PF_OK: return "PF_OK";
+        case PF_ERR_INVALID_ARG: return "PF_ERR_INVALID_ARG";
+        case PF_ERR_UNSUPPORTED: return "PF_ERR_UNSUPPORTED";
+        case PF_ERR_CUDA: return "PF_ERR_CUDA";
+        case PF_ERR_DEVICE_BOUNDS: return "PF_ERR_DEVICE_BOUNDS";
+        case PF_ERR_DEVICE_TIMEOUT: return "PF_ERR_DEVICE_TIMEOUT";
+        default: return "PF_UNKNOWN_STATUS";
+    }
+}
+
+pf_status pf_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping, void* k_cache,
+                               void* v_cache, int64_t num_tokens, int num_kv_heads, int head_dim, int block_size,
+                               int64_t num_blocks, pf_stream_t stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PF_ERR_INVALID_ARG;
+    if (head_dim % 8 != 0) return PF_ERR_UNSUPPORTED;
+    const size_t cache_elems =
+        mul_sat(mul_sat(mul_sat(size_t(num_blocks), size_t(num_kv_heads)), size_t(block_size)), size_t(head_dim));
+    const size_t in_elems = mul_sat(mul_sat(size_t(num_tokens), size_t(num_kv_heads)), size_t(head_dim));
+    if (cache_elems >= (SIZE_MAX >> 2) || in_elems >= (SIZE_MAX >> 2) ||
+        (long long)num_kv_heads * (head_dim / 8) > INT32_MAX)
+        return PF_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PF_OK;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return PF_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    int sms = 0;
+    if (error_word(&err) != cudaSuccess || sm_count(&sms) != cudaSuccess) return PF_ERR_CUDA;
+    const long long total = (long long)num_tokens * num_kv_heads * (head_dim / 8);
+    const long long want = (total + 255) / 256;
+    const unsigned blocks = unsigned(want < (long long)sms * 16 ? want : (long long)sms * 16);
+    reshape_and_cache_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, static_cast<uint4*>(k_cache),
+        static_cast<uint4*>(v_cache), total, num_kv_heads, head_dim / 8, block_size,
+        (long long)num_blocks * block_size, err);
+    return cudaGetLastError() == cudaSuccess ? PF_OK : PF_ERR_CUDA;
+}
+
+pf_status pf_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                    int max_blocks_per_seq, int64_t num_blocks, float scale, float* out,
+                                    pf_stream_t stream) {
+    const AttnArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, max_blocks_per_seq, num_blocks, scale};
+    pf_status st = check_attention(a);
+    if (st != PF_OK) return st;
+    if (num_seqs == 0) return PF_OK;
+    if (!aligned(out, 16)) return PF_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
+    DecodeParams p = make_params(a, err);
+    p.out = out;
+    const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, false,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
+}
+
+size_t pf_paged_attention_partition_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
+                                                     int max_context_len, int partition_size,
+                                                     size_t* tmp_out_offset, size_t* tmp_m_offset,
+                                                     size_t* tmp_l_offset) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_size <= 0)
+        return 0;
+    const size_t np = max_context_len > 0 ? (size_t(max_context_len) + partition_size - 1) / partition_size : 1;
+    const size_t n = mul_sat(mul_sat(size_t(num_seqs), size_t(num_q_heads)), np);
+    const size_t out_elems = mul_sat(n, size_t(head_dim));
+    if (out_elems >= (SIZE_MAX >> 4)) return 0;
+    const size_t out_bytes = round_up(out_elems * 4, 256);
+    const size_t ml_bytes = round_up(n * 4, 256);
+    if (tmp_out_offset) *tmp_out_offset = 0;
+    if (tmp_m_offset) *tmp_m_offset = out_bytes;
+    if (tmp_l_offset) *tmp_l_offset = out_bytes + ml_bytes;
+    return out_bytes + 2 * ml_bytes;
+}
+
+size_t pf_paged_attention_partition_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                                   int max_context_len, int partition_size) {
+    return pf_paged_attention_partition_workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len,
+                                                         partition_size, nullptr, nullptr, nullptr);
+}
+
+pf_status pf_paged_attention_decode_partition(const void* q, const void* k_cache, const void* v_cache,
+                                              const int32_t* block_tables, const int32_t* context_lens,
+                                              int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                              int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                              float scale, int partition_size, int max_context_len,
+                                              void* workspace, size_t workspace_bytes, pf_stream_t stream) {
+    const AttnArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, max_blocks_per_seq, num_blocks, scale};
+    pf_status st = check_attention(a);
+    if (st != PF_OK) return st;
+    if (partition_size <= 0 || max_context_len < 0) return PF_ERR_INVALID_ARG;
+    if (partition_size % kTileTokens != 0) return PF_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PF_OK;
+    size_t off_o = 0, off_m = 0, off_l = 0;
+    const size_t need = pf_paged_attention_partition_workspace_layout(num_seqs, num_q_heads, head_dim,
+                                                                      max_context_len, partition_size, &off_o,
+                                                                      &off_m, &off_l);
+    if (need == 0 || workspace_bytes < need || !aligned(workspace, 256)) return PF_ERR_INVALID_ARG;
+    const long long np = max_context_len > 0 ? ((long long)max_context_len + partition_size - 1) / partition_size : 1;
+    if (np * num_kv_heads * num_seqs > INT32_MAX) return PF_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
+    DecodeParams p = make_params(a, err);
+    char* ws = static_cast<char*>(workspace);
+    p.out = reinterpret_cast<float*>(ws + off_o);
+    p.part_m = reinterpret_cast<float*>(ws + off_m);
+    p.part_l = reinterpret_cast<float*>(ws + off_l);
+    p.partition_size = partition_size;
+    p.num_partitions = int(np);
+    p.max_context_len = max_context_len;
+    const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, true,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
+}
+
+pf_status pf_paged_attention_merge(const void* workspace, const int32_t* context_lens, int num_seqs,
+                                   int num_q_heads, int head_dim, int partition_size, int max_context_len,
+                                   float* out, pf_stream_t stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || partition_size <= 0 || max_context_len < 0)
+        return PF_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PF_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PF_OK;
+    if (!aligned(workspace, 256) || !aligned(context_lens, 4) || !aligned(out, 16)) return PF_ERR_INVALID_ARG;
+    size_t off_o = 0, off_m = 0, off_l = 0;
+    if (pf_paged_attention_partition_workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len,
+                                                      partition_size, &off_o, &off_m, &off_l) == 0)
+        return PF_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
+    const int np = max_context_len > 0 ? int(((long long)max_context_len + partition_size - 1) / partition_size) : 1;
+    const char* ws = static_cast<const char*>(workspace);
+    const long long warps = (long long)num_seqs * num_q_heads;
+    const unsigned blocks = unsigned((warps + 7) / 8);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const float* to = reinterpret_cast<const float*>(ws + off_o);
+    const float* tm = reinterpret_cast<const float*>(ws + off_m);
+    const float* tl = reinterpret_cast<const float*>(ws + off_l);
+    if (head_dim == 64)
+        lse_merge_kernel<64><<<blocks, 256, 0, s>>>(to, tm, tl, context_lens, num_seqs, num_q_heads, partition_size,
+                                                    np, max_context_len, out, err);
+    else
+        lse_merge_kernel<128><<<blocks, 256, 0, s>>>(to, tm, tl, context_lens, num_seqs, num_q_heads,
+                                                     partition_size, np, max_context_len, out, err);
+    return cudaGetLastError() == cudaSuccess ? PF_OK : PF_ERR_CUDA;
+}
+
+pf_status pf_get_device_error(pf_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned* err = nullptr;
+    if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PF_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpyAsync(&word, err, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PF_ERR_CUDA;
+    if (cudaMemsetAsync(err, 0, sizeof word, s) != cudaSuccess) return PF_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PF_ERR_CUDA;
+    if (word & ERR_TIMEOUT) return PF_ERR_DEVICE_TIMEOUT;
+    if (word & ERR_BOUNDS) return PF_ERR_DEVICE_BOUNDS;
+    return PF_OK;
+}
+
+pf_status pf_debug_bounded_wait(int64_t limit_ns, pf_stream_t stream) {
+    if (limit_ns < 1000 || limit_ns > 10000000000LL) return PF_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
+    bounded_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err, (unsigned long long)limit_ns);
+    return cudaGetLastError() == cudaSuccess ? PF_OK : PF_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,454 @@
+// Paged-KV decode attention kernel (single pass and context-partition pass).
+//
+// Method: decode-phase attention that reads K/V straight out of physical KV
+// blocks through a per-sequence block table with an online softmax and
+// grouped-query heads (ForgeLLM README, feature list: "Physical KV blocks with
+// logical per-request block tables", "Decode-only block-table attention reads
+// physical KV blocks directly ... online softmax without constructing padded
+// batch-wide K/V", "grouped-query attention"), with warp-shuffle max / sum
+// reductions (LLM-Inference-Engine README, "Flash Attention CUDA Kernel ...
+// warp-level shuffle reductions").  The split over context partitions with a
+// log-sum-exp merge is the flash-decoding decomposition of the same sums.
+//
+// GB300 design:
+//  * One CTA owns one (sequence, kv head [, partition]) item and all G query
+//    heads that share the kv head, so each K/V byte is read from HBM once.
+//  * The cache layout [block, kv head, token, dim] makes every (block, kv head)
+//    tile contiguous; a tile of 16 tokens (2 KiB for D=64, 4 KiB for D=128, for
+//    each of K and V) moves with one cp.async.bulk per operand into shared
+//    memory, completing on an mbarrier.  Only the valid rows of a sequence's
+//    last tile are copied.
+//  * Each warp is an independent streamer: it takes every NW-th tile of the
+//    item, keeps NST tiles in flight in a private ring, and lane 0 issues the
+//    copies, prefetching block-table entries NST+2 tiles ahead.
+//  * Scores: lanes split each 16-token tile as (token, 16-byte chunk); a lane
+//    holds its chunk of all G query rows in fp32 registers (64 values), so the
+//    G dot products cost one shared-memory read per chunk.  Chunk order is
+//    rotated per token so the 8 lanes of a shared-memory phase hit distinct
+//    banks.  A reduce-scatter over the lanes of a token leaves one finished
+//    score per lane.
+//  * fp32 online softmax in base 2 (scale*log2(e) folded in), warp-shuffle max
+//    and sum; probabilities go through a warp-private shared buffer to the
+//    P.V step, where each lane owns D/32 output dims of all G heads.
+//  * The NW warps of a CTA merge their (m, l, acc) in shared memory at the end.
+//  * No trap, no unbounded spin: every mbarrier wait is bounded; a bad table
+//    entry or length sets the device error word and NaN-fills the item's rows.
+#pragma once
+
+#include <atomic>
+#include <cmath>
+
+#include "pf_device.cuh"
+#include "pf_internal.h"
+
+namespace pf {
+
+template <int D, int G>
+struct DecodeGeometry {
+    static_assert(D == 64 || D == 128, "head_dim");
+    static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group");
+    static constexpr int TT = kTileTokens;
+    static constexpr int ROW_BYTES = D * 2;
+    static constexpr int TILE_BYTES = TT * ROW_BYTES;        // one K (or V) tile
+    static constexpr int CHUNKS_PER_ROW = D / 8;             // 16-byte chunks in a token row
+    static constexpr int LPT = (G * D / 64) > 2 ? (G * D / 64) : 2;  // lanes per token (scores)
+    static constexpr int TPP = 32 / LPT;                     // tokens per score pass
+    static constexpr int NPASS = TT / TPP;                   // score passes per tile
+    static constexpr int CPL = CHUNKS_PER_ROW / LPT;         // chunks per lane per row
+    static constexpr int DUP = LPT / G;                      // lanes left holding the same score
+    static constexpr int DPL = D / 32;                       // output dims per lane (P.V)
+    static constexpr int ROT_MOD = LPT < 8 ? 8 / LPT : 1;    // tokens sharing a smem phase
+    static constexpr int PSM = TT * G + G;                   // probabilities + per-head alpha
+    static constexpr int PSM_PAD = (PSM + 3) & ~3;
+    static_assert(CPL * LPT == CHUNKS_PER_ROW && NPASS * TPP == TT, "geometry");
+};
+
+template <int D, int G, int NW, int NST>
+constexpr size_t decode_smem_bytes() {
+    using Geo = DecodeGeometry<D, G>;
+    return size_t(NW) * NST * 2 * Geo::TILE_BYTES      // K/V stages
+           + size_t(NW) * Geo::PSM_PAD * 4             // probabilities, alpha; then m, l
+           + 16                                        // per-warp failure flags (NW <= 4)
+           + size_t(NW) * NST * 8;                     // mbarriers
+}
+
+// Sum of v[0..G-1] over the LPT lanes of one token, spread so that afterwards
+// lane slice `sl` holds the full sum of head sl / DUP in v[0].
+template <int G, int LPT>
+__device__ __forceinline__ float reduce_scatter_heads(float (&v)[G], int sl) {
+#pragma unroll
+    for (int n = G, m = LPT / 2; n > 1; n >>= 1, m >>= 1) {
+        const bool upper = (sl & m) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = upper ? v[i] : v[i + n / 2];
+            const float keep = upper ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(FULL_MASK, send, m);
+        }
+    }
+#pragma unroll
+    for (int m = (LPT / G) / 2; m >= 1; m >>= 1) v[0] += __shfl_xor_sync(FULL_MASK, v[0], m);
+    return v[0];
+}
+
+template <int G>
+__device__ __forceinline__ void load_probs(const float* src, float (&pw)[G]) {
+    if constexpr (G == 1) {
+        pw[0] = src[0];
+    } else if constexpr (G == 2) {
+        const float2 a = *reinterpret_cast<const float2*>(src);
+        pw[0] = a.x; pw[1] = a.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < G; i += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(src + i);
+            pw[i] = a.x; pw[i + 1] = a.y; pw[i + 2] = a.z; pw[i + 3] = a.w;
+        }
+    }
+}
+
+template <int D, int G, int NW, int NST, bool PART>
+__global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParams p) {
+    using Geo = DecodeGeometry<D, G>;
+    constexpr int TT = Geo::TT, LPT = Geo::LPT, TPP = Geo::TPP, NPASS = Geo::NPASS, CPL = Geo::CPL;
+    constexpr int DUP = Geo::DUP, DPL = Geo::DPL, ROW = Geo::ROW_BYTES, TILE = Geo::TILE_BYTES;
+    constexpr int PSM_PAD = Geo::PSM_PAD;
+    constexpr int R = NST + 2;  // table entries lane 0 holds ahead of the copies
+    static_assert(NW <= 4, "flag area holds 4 warps");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    float* psm_all = reinterpret_cast<float*>(smem + size_t(NW) * NST * 2 * TILE);
+    int* flags = reinterpret_cast<int*>(psm_all + NW * PSM_PAD);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(flags) + 16);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tp = lane / LPT, sl = lane % LPT;
+    const int hh = sl / DUP;                 // head (within the group) of this lane's scores
+    const int rot = tp % Geo::ROT_MOD;
+    const bool writer = (sl % DUP) == 0;     // one lane per (head, token) writes shared state
+
+    // ---- which item
+    int seq, kvh, part = 0;
+    if constexpr (PART) {
+        part = blockIdx.x % p.num_partitions;
+        const int rest = blockIdx.x / p.num_partitions;
+        kvh = rest % p.num_kv_heads;
+        seq = rest / p.num_kv_heads;
+    } else {
+        kvh = blockIdx.x % p.num_kv_heads;
+        seq = blockIdx.x / p.num_kv_heads;
+    }
+    const int Hq = p.num_q_heads;
+    const int qh0 = kvh * G;
+    const int L = __ldg(p.context_lens + seq);
+    bool len_bad = L < 0 || (long long)L > (long long)p.max_blocks_per_seq * p.block_size;
+    int t0 = 0, t1 = L;
+    if constexpr (PART) {
+        len_bad = len_bad || L > p.max_context_len;
+        t0 = part * p.partition_size;
+        if (!len_bad && t0 >= L) return;  // empty partition: the merge never reads it
+        t1 = min(L, t0 + p.partition_size);
+    }
+    if (len_bad) {
+        if (threadIdx.x == 0) set_error(p.err, ERR_BOUNDS);
+        for (int e = threadIdx.x; e < G * D; e += NW * 32) {
+            const int h = e / D, d = e % D;
+            if constexpr (PART) {
+                const size_t slot = (size_t(seq) * Hq + qh0 + h) * p.num_partitions + part;
+                p.out[slot * D + d] = NAN;
+                if (d == 0) { p.part_m[slot] = NAN; p.part_l[slot] = NAN; }
+            } else {
+                p.out[(size_t(seq) * Hq + qh0) * D + e] = NAN;
+            }
+        }
+        return;
+    }
+
+    // ---- this warp's tiles: ti0 + warp + k*NW, k < nk
+    const int ti0 = t0 / TT;
+    const int ntiles = (t1 - t0 + TT - 1) / TT;
+    const int nk = ntiles > warp ? (ntiles - warp + NW - 1) / NW : 0;
+
+    unsigned char* my_stages = smem + size_t(warp) * NST * 2 * TILE;
+    const uint32_t stage0 = smem_u32(my_stages);
+    const uint32_t bar0 = smem_u32(bars + warp * NST);
+    float* psm = psm_all + warp * PSM_PAD;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < NST; ++s) mbar_init(bar0 + 8 * s, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+
+    // ---- producer state (lane 0)
+    const int32_t* trow = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
+    const int bs = p.block_size, bshift = p.block_shift;
+    auto block_index = [&](int tok) { return bshift >= 0 ? (tok >> bshift) : (tok / bs); };
+    auto block_offset = [&](int tok) { return bshift >= 0 ? (tok & (bs - 1)) : (tok % bs); };
+    auto tile_token = [&](int k) { return (ti0 + warp + k * NW) * TT; };
+    int ent[R];
+    bool bad_block = false;
+    const uint64_t policy = l2_policy_evict_first();
+
+    auto issue = [&](int k, int pb) {
+        const int s = k % NST;
+        const uint32_t bar = bar0 + 8 * s;
+        const int tok = tile_token(k);
+        if (pb >= 0 && (long long)pb < p.num_blocks) {
+            const uint32_t bytes = uint32_t(min(TT, t1 - tok)) * ROW;
+            const size_t row = (size_t(pb) * p.num_kv_heads + kvh) * size_t(bs) + block_offset(tok);
+            const uint32_t dst = stage0 + uint32_t(s) * 2 * TILE;
+            mbar_arrive_expect_tx(bar, 2 * bytes);
+            bulk_copy_g2s(dst, p.k_cache + row * D, bytes, bar, policy);
+            bulk_copy_g2s(dst + TILE, p.v_cache + row * D, bytes, bar, policy);
+        } else {
+            bad_block = true;   // no copy: the stage keeps stale data, the rows end up NaN
+            mbar_arrive(bar);
+        }
+    };
+    auto advance = [&](int k_next_load) {  // shift the table window after an issue
+#pragma unroll
+        for (int j = 0; j < R - 1; ++j) ent[j] = ent[j + 1];
+        ent[R - 1] = k_next_load < nk ? __ldg(trow + block_index(tile_token(k_next_load))) : 0;
+    };
+    if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) ent[j] = j < nk ? __ldg(trow + block_index(tile_token(j))) : 0;
+#pragma unroll
+        for (int k = 0; k < NST; ++k) {
+            if (k < nk) {
+                issue(k, ent[0]);
+                advance(k + R);
+            }
+        }
+    }
+
+    // ---- this lane's slice of the G query rows, fp32, in its chunk-read order
+    float2 qf[G][CPL][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const uint16_t* qrow = p.q + (size_t(seq) * Hq + qh0 + h) * D;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const int chunk = sl + LPT * ((j + rot) % CPL);
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(qrow + chunk * 8));
+            qf[h][j][0] = bf16x2_to_float2(w.x);
+            qf[h][j][1] = bf16x2_to_float2(w.y);
+            qf[h][j][2] = bf16x2_to_float2(w.z);
+            qf[h][j][3] = bf16x2_to_float2(w.w);
+        }
+    }
+    int kofs[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) kofs[j] = tp * ROW + (sl + LPT * ((j + rot) % CPL)) * 16;
+
+    float m_run = -INFINITY, l_run = 0.f;
+    float2 acc[G][DPL / 2];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < DPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
+
+    bool timed_out = false;
+    int k = 0;
+    for (; k < nk; ++k) {
+        const int s = k % NST;
+        const bool ok = mbar_wait_bounded(bar0 + 8 * s, (k / NST) & 1, p.wait_limit_ns);
+        if (__any_sync(FULL_MASK, !ok)) { timed_out = true; break; }
+        const unsigned char* Ks = my_stages + size_t(s) * 2 * TILE;
+        const unsigned char* Vs = Ks + TILE;
+        const int nvalid = min(TT, t1 - tile_token(k));
+
+        // -- scores of this lane's tokens for head hh, base-2 units
+        float sc[NPASS];
+#pragma unroll
+        for (int pass = 0; pass < NPASS; ++pass) {
+            const unsigned char* rowp = Ks + pass * TPP * ROW;
+            float2 a[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) a[h] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                const uint4 w = *reinterpret_cast<const uint4*>(rowp + kofs[j]);
+                const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
+                const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    a[h] = ffma2(qf[h][j][0], k0, a[h]);
+                    a[h] = ffma2(qf[h][j][1], k1, a[h]);
+                    a[h] = ffma2(qf[h][j][2], k2, a[h]);
+                    a[h] = ffma2(qf[h][j][3], k3, a[h]);
+                }
+            }
+            float v[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) v[h] = a[h].x + a[h].y;
+            const float dot = reduce_scatter_heads<G, LPT>(v, sl);
+            sc[pass] = (pass * TPP + tp < nvalid) ? dot * p.scale_log2 : -INFINITY;
+        }
+
+        // -- online softmax for head hh
+        float mx = sc[0];
+#pragma unroll
+        for (int pass = 1; pass < NPASS; ++pass) mx = fmaxf(mx, sc[pass]);
+#pragma unroll
+        for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, o));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = exp2_approx(m_run - m_new);
+        float psum = 0.f;
+#pragma unroll
+        for (int pass = 0; pass < NPASS; ++pass) {
+            const float pv = exp2_approx(sc[pass] - m_new);
+            psum += pv;
+            if (writer) psm[(pass * TPP + tp) * G + hh] = pv;
+        }
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+        if (writer && tp == 0) psm[TT * G + hh] = alpha;
+        __syncwarp();
+
+        // -- acc = alpha * acc + sum_t p_t V_t, lane owns dims [lane*DPL, lane*DPL + DPL)
+        {
+            float al[G];
+            load_probs<G>(psm + TT * G, al);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < DPL / 2; ++e) {
+                    acc[h][e].x *= al[h];
+                    acc[h][e].y *= al[h];
+                }
+        }
+        auto pv_step = [&](int t) {
+            float pw[G];
+            load_probs<G>(psm + t * G, pw);
+            float2 vv[DPL / 2];
+            if constexpr (DPL == 4) {
+                const uint2 w = *reinterpret_cast<const uint2*>(Vs + t * ROW + lane * 8);
+                vv[0] = bf16x2_to_float2(w.x);
+                vv[1] = bf16x2_to_float2(w.y);
+            } else {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + t * ROW + lane * 4);
+                vv[0] = bf16x2_to_float2(w);
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < DPL / 2; ++e) acc[h][e] = ffma2(make_float2(pw[h], pw[h]), vv[e], acc[h][e]);
+        };
+        if (nvalid == TT) {
+#pragma unroll
+            for (int t = 0; t < TT; ++t) pv_step(t);
+        } else {
+            for (int t = 0; t < nvalid; ++t) pv_step(t);  // rows past the length are never read
+        }
+        __syncwarp();
+
+        // -- refill the stage just drained
+        if (lane == 0 && k + NST < nk) {
+            issue(k + NST, ent[0]);
+            advance(k + NST + R);
+        }
+    }
+
+    if (timed_out) {
+        // give the copies still in flight a bounded chance to land before the
+        // shared memory is reused, then report
+        if (lane == 0) set_error(p.err, ERR_TIMEOUT);
+        const int last = min(k + NST, nk);
+        for (int kk = k; kk < last; ++kk) mbar_wait_bounded(bar0 + 8 * (kk % NST), (kk / NST) & 1, p.wait_limit_ns);
+    }
+    if (lane == 0 && bad_block) set_error(p.err, ERR_BOUNDS);
+    const bool warp_failed = __any_sync(FULL_MASK, bad_block || timed_out);
+
+    // ---- per-head sum of l over the lanes holding that head
+#pragma unroll
+    for (int o = LPT; o < 32; o <<= 1) l_run += __shfl_xor_sync(FULL_MASK, l_run, o);
+
+    // ---- stash (m, l, acc) of this warp; its stage memory and psm are free now
+    __syncwarp();
+    if (writer && tp == 0) {
+        psm[hh] = m_run;
+        psm[G + hh] = l_run;
+    }
+    float* accs = reinterpret_cast<float*>(my_stages);
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < DPL / 2; ++e)
+            *reinterpret_cast<float2*>(accs + h * D + lane * DPL + 2 * e) = acc[h][e];
+    if (lane == 0) flags[warp] = warp_failed ? 1 : 0;
+    __syncthreads();
+
+    // ---- merge the NW warps and write out
+    bool failed = false;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) failed = failed || flags[w] != 0;
+    for (int e = threadIdx.x; e < G * D; e += NW * 32) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, psm_all[w * PSM_PAD + h]);
+        float wsum = 0.f, o = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float f = exp2_approx(psm_all[w * PSM_PAD + h] - M);
+                const float* accw = reinterpret_cast<const float*>(smem + size_t(w) * NST * 2 * TILE);
+                wsum += f * psm_all[w * PSM_PAD + G + h];
+                o += f * accw[h * D + d];
+            }
+        }
+        float res = wsum > 0.f ? o / wsum : 0.f;
+        if (failed) res = NAN;
+        if constexpr (PART) {
+            const size_t slot = (size_t(seq) * Hq + qh0 + h) * p.num_partitions + part;
+            p.out[slot * D + d] = res;
+            if (d == 0) {
+                p.part_m[slot] = failed ? NAN : M * 0.6931471805599453f;
+                p.part_l[slot] = failed ? NAN : wsum;
+            }
+        } else {
+            p.out[(size_t(seq) * Hq + qh0) * D + e] = res;
+        }
+    }
+}
+
+template <int D, int G, int NW, int NST, bool PART>
+cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream) {
+    constexpr size_t smem = decode_smem_bytes<D, G, NW, NST>();
+    auto kern = paged_decode_kernel<D, G, NW, NST, PART>;
+    static std::atomic<unsigned long long> configured{0};  // one bit per device ordinal
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit == 0 || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const long long grid = PART ? (long long)p.num_partitions * p.num_kv_heads * p.num_seqs
+                                : (long long)p.num_seqs * p.num_kv_heads;
+    if (grid <= 0) return cudaSuccess;
+    kern<<<unsigned(grid), NW * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, int NW, int NST>
+cudaError_t launch_decode_for_dim(const DecodeParams& p, int group, bool partition, cudaStream_t stream) {
+    switch (group) {
+        case 1: return partition ? launch_decode_variant<D, 1, NW, NST, true>(p, stream)
+                                 : launch_decode_variant<D, 1, NW, NST, false>(p, stream);
+        case 2: return partition ? launch_decode_variant<D, 2, NW, NST, true>(p, stream)
+                                 : launch_decode_variant<D, 2, NW, NST, false>(p, stream);
+        case 4: return partition ? launch_decode_variant<D, 4, NW, NST, true>(p, stream)
+                                 : launch_decode_variant<D, 4, NW, NST, false>(p, stream);
+        case 8: return partition ? launch_decode_variant<D, 8, NW, NST, true>(p, stream)
+                                 : launch_decode_variant<D, 8, NW, NST, false>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pf

@@ -1,0 +1,11 @@
+// head_dim = 128 instantiations of the decode / partition kernel:
+// 4 warps per CTA, 3 stages of 16-token K+V tiles (8 KiB) per warp, two CTAs per SM.
+#include "pf_decode.cuh"
+
+namespace pf {
+
+cudaError_t launch_decode_d128(const DecodeParams& p, int group, bool partition, cudaStream_t stream) {
+    return launch_decode_for_dim<128, 4, 3>(p, group, partition, stream);
+}
+
+}  // namespace pf

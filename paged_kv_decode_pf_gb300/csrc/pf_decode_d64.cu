@@ -1,0 +1,11 @@
+// head_dim = 64 instantiations of the decode / partition kernel:
+// 4 warps per CTA, 4 stages of 16-token K+V tiles (4 KiB) per warp.
+#include "pf_decode.cuh"
+
+namespace pf {
+
+cudaError_t launch_decode_d64(const DecodeParams& p, int group, bool partition, cudaStream_t stream) {
+    return launch_decode_for_dim<64, 4, 4>(p, group, partition, stream);
+}
+
+}  // namespace pf

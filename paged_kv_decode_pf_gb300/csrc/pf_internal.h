@@ -1,0 +1,48 @@
+// Host-side interfaces between the C ABI (pf_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pf {
+
+// Tokens per K/V tile that one bulk copy moves; block_size and the partition
+// size must be multiples of it.
+constexpr int kTileTokens = 16;
+
+// Arguments of the decode / partition kernel; see pf.h for the meaning of each.
+struct DecodeParams {
+    const uint16_t* q;
+    const uint16_t* k_cache;
+    const uint16_t* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float* out;        // decode: out [S, Hq, D]; partition pass: tmp_out [S, Hq, NP, D]
+    float* part_m;     // partition pass only: tmp_m [S, Hq, NP] (natural-log units)
+    float* part_l;     // partition pass only: tmp_l [S, Hq, NP]
+    unsigned* err;     // device error word
+    long long num_blocks;
+    unsigned long long wait_limit_ns;
+    float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int block_size;          // a multiple of 16
+    int block_shift;         // log2(block_size) when it is a power of two, else -1
+    int max_blocks_per_seq;
+    int partition_size;      // partition pass: tokens per partition (multiple of 16)
+    int num_partitions;      // partition pass: NP
+    int max_context_len;     // partition pass: bound every context length must respect
+};
+
+// Launch the single-pass decode kernel (partition == false) or the partition
+// pass (partition == true) for one head_dim.  Returns cudaSuccess or the launch error.
+cudaError_t launch_decode_d64(const DecodeParams& p, int group, bool partition, cudaStream_t stream);
+cudaError_t launch_decode_d128(const DecodeParams& p, int group, bool partition, cudaStream_t stream);
+
+// Default bound of every device-side wait: long enough never to fire on a
+// healthy GPU (a tile copy takes microseconds), short enough to end a broken call.
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+
+}  // namespace pf

@@ -53,3 +53,29 @@ def check_close(got, ref, abs_tol=2e-3, rel_tol=1e-2, rel_floor=0.2):
     max_rel = float((d[big] / np.abs(ref[big])).max()) if big.any() else 0.0
     assert max_abs <= abs_tol and max_rel <= rel_tol, f"max_abs={max_abs:.3e} max_rel={max_rel:.3e}"
     return max_abs, max_rel
+
+
+def to_device(wl, device="cuda"):
+    """The workload's arrays as CUDA tensors (bf16 tensors carry the same bits)."""
+    import torch
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    d = dict(q=bf(wl.q), k_cache=bf(wl.k_cache), v_cache=bf(wl.v_cache),
+             block_tables=torch.from_numpy(np.ascontiguousarray(wl.block_tables)).to(device),
+             context_lens=torch.from_numpy(np.ascontiguousarray(wl.context_lens)).to(device))
+    if wl.slot_mapping is not None:
+        d.update(new_k=bf(wl.new_k), new_v=bf(wl.new_v),
+                 slot_mapping=torch.from_numpy(np.ascontiguousarray(wl.slot_mapping)).to(device))
+    return d
+
+
+def bits(t):
+    """bf16 CUDA tensor -> uint16 numpy array of its bits."""
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def attn_args(d):
+    return d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"]

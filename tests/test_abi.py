@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: libpf.so builds for sm_103a, loads, exports every function that
+include/pf.h declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pf.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_decode_pf_gb300 import _build
+    _build.build()
+    import paged_kv_decode_pf_gb300 as pf
+    return pf.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^PF_API\s+[\w\s\*]+?\b(pf_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_abi():
+    names = set(declared_functions())
+    assert {"pf_reshape_and_cache", "pf_paged_attention_decode", "pf_paged_attention_decode_partition",
+            "pf_paged_attention_merge", "pf_paged_attention_partition_workspace_size",
+            "pf_get_device_error", "pf_status_string"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_only_declared_symbols_are_exported(lib):
+    import subprocess
+    from paged_kv_decode_pf_gb300 import LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert {n for n in exported if n.startswith("pf_")} == set(declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    import paged_kv_decode_pf_gb300 as pf
+    for code, name in pf.STATUS_NAMES.items():
+        assert lib.pf_status_string(code).decode() == name
+    assert re.fullmatch(r"\d+\.\d+\.\d+", pf.version())
+
+
+def test_workspace_layout_arithmetic(lib):
+    import paged_kv_decode_pf_gb300 as pf
+    r = lambda x: (x + 255) // 256 * 256
+    for S, Hq, D, mx, P in [(4, 32, 128, 131072, 512), (1, 1, 64, 1, 16), (3, 8, 64, 0, 32), (7, 5, 128, 1000, 48)]:
+        NP = max(1, -(-mx // P))
+        total, oo, om, ol = pf.partition_workspace_layout(S, Hq, D, mx, P)
+        assert (oo, om, ol) == (0, r(S * Hq * NP * D * 4), r(S * Hq * NP * D * 4) + r(S * Hq * NP * 4))
+        assert total == ol + r(S * Hq * NP * 4)
+        assert lib.pf_paged_attention_partition_workspace_size(S, Hq, D, mx, P) == total
+    for bad in [(0, 1, 64, 10, 16), (1, 0, 64, 10, 16), (1, 1, 64, -1, 16), (1, 1, 64, 10, 0)]:
+        assert pf.partition_workspace_layout(*bad)[0] == 0
+
+
+def _decode(lib, **kw):
+    a = dict(q=0x10000, kc=0x20000, vc=0x30000, bt=0x40000, cl=0x50000, S=2, Hq=8, Hkv=2, D=128, bs=16, MB=4,
+             NB=64, scale=0.125, out=0x60000)
+    a.update(kw)
+    return lib.pf_paged_attention_decode(a["q"], a["kc"], a["vc"], a["bt"], a["cl"], a["S"], a["Hq"], a["Hkv"],
+                                         a["D"], a["bs"], a["MB"], a["NB"], a["scale"], a["out"], None)
+
+
+@pytest.mark.parametrize("change,want", [
+    (dict(S=-1), 1), (dict(Hq=0), 1), (dict(Hkv=0), 1), (dict(Hq=6, Hkv=4), 1), (dict(D=0), 1),
+    (dict(bs=0), 1), (dict(MB=0), 1), (dict(NB=0), 1), (dict(NB=2 ** 31), 1), (dict(scale=float("inf")), 1),
+    (dict(q=None), 1), (dict(q=0x10002), 1), (dict(bt=0x40002), 1), (dict(out=0x60004), 1),
+    (dict(D=96), 2), (dict(D=256), 2), (dict(bs=8), 2), (dict(bs=24), 2), (dict(Hq=32, Hkv=2), 2),
+    (dict(Hq=6, Hkv=2), 2),
+])
+def test_decode_host_validation(lib, change, want):
+    assert _decode(lib, **change) == want
+
+
+def test_zero_sequences_is_a_no_op(lib):
+    assert _decode(lib, S=0, q=None, kc=None, vc=None, bt=None, cl=None, out=None) == 0
+
+
+def test_partition_and_merge_host_validation(lib):
+    P = ctypes.c_void_p
+    args = [0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 2, 8, 2, 128, 16, 4, 64, ctypes.c_float(0.1)]
+    f = lib.pf_paged_attention_decode_partition
+    assert f(*args, 0, 64, P(0x70000), 1 << 20, None) == 1          # partition size 0
+    assert f(*args, 24, 64, P(0x70000), 1 << 20, None) == 2         # not a multiple of 16
+    assert f(*args, 32, -1, P(0x70000), 1 << 20, None) == 1         # negative max length
+    assert f(*args, 32, 64, P(0x70000), 16, None) == 1              # workspace too small
+    assert f(*args, 32, 64, P(0x70010), 1 << 20, None) == 1         # workspace misaligned
+    m = lib.pf_paged_attention_merge
+    assert m(P(0x70000), P(0x50000), 2, 8, 96, 32, 64, P(0x60000), None) == 2
+    assert m(P(0x70000), P(0x50000), 2, 8, 128, 0, 64, P(0x60000), None) == 1
+    assert m(P(0x70010), P(0x50000), 2, 8, 128, 32, 64, P(0x60000), None) == 1
+    assert m(None, None, 0, 8, 128, 32, 64, None, None) == 0
+
+
+def test_append_host_validation(lib):
+    f = lib.pf_reshape_and_cache
+    ok = [0x10000, 0x20000, 0x30000, 0x40000, 0x50000]
+    assert f(*ok, -1, 2, 64, 16, 10, None) == 1
+    assert f(*ok, 4, 2, 60, 16, 10, None) == 2                      # head_dim not a multiple of 8
+    assert f(*ok, 4, 2, 64, 0, 10, None) == 1
+    assert f(0x10008, *ok[1:], 4, 2, 64, 16, 10, None) == 1         # misaligned k
+    assert f(*ok[:2], 0x30004, *ok[3:], 4, 2, 64, 16, 10, None) == 1  # misaligned slot_mapping
+    assert f(None, None, None, None, None, 0, 2, 64, 16, 10, None) == 0
+
+
+def test_debug_wait_limits(lib):
+    assert lib.pf_debug_bounded_wait(10, None) == 1
+    assert lib.pf_debug_bounded_wait(10 ** 11, None) == 1
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    import paged_kv_decode_pf_gb300 as pf
+    monkeypatch.setattr(pf, "_LIB", None)
+    monkeypatch.setattr(pf, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        pf.lib()
