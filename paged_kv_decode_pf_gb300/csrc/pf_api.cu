@@ -89,65 +89,87 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __r
 
 // ------------------------------------------------------------------- merge
 
-// One warp per (sequence, query head): log-sum-exp merge of its partitions.
+// One CTA of MERGE_WARPS warps per (sequence, query head): log-sum-exp merge of
+// its partitions.  The maximum and the weight sum are reduced over the whole
+// CTA; the warps then take every MERGE_WARPS-th partition (lanes own D/32
+// dims, four partitions in flight per warp) and add their sums in shared memory.
+constexpr int MERGE_WARPS = 4;
+
 template <int D>
-__global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict__ tmp_out,
-                                                        const float* __restrict__ tmp_m,
-                                                        const float* __restrict__ tmp_l,
-                                                        const int32_t* __restrict__ context_lens, int num_seqs,
-                                                        int num_q_heads, int partition_size,
-                                                        int num_partitions, int max_context_len,
-                                                        float* __restrict__ out, unsigned* err) {
+__global__ void __launch_bounds__(MERGE_WARPS * 32) lse_merge_kernel(const float* __restrict__ tmp_out,
+                                                                     const float* __restrict__ tmp_m,
+                                                                     const float* __restrict__ tmp_l,
+                                                                     const int32_t* __restrict__ context_lens,
+                                                                     int num_seqs, int num_q_heads,
+                                                                     int partition_size, int num_partitions,
+                                                                     int max_context_len, float* __restrict__ out,
+                                                                     unsigned* err) {
     constexpr int DPL = D / 32;
+    constexpr int NT = MERGE_WARPS * 32;
     constexpr float kLog2e = 1.4426950408889634f;
-    const long long gw = blockIdx.x * (long long)(blockDim.x / 32) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= (long long)num_seqs * num_q_heads) return;
-    const int seq = int(gw / num_q_heads);
+    __shared__ float red[MERGE_WARPS];
+    __shared__ __align__(16) float accs[MERGE_WARPS][D];
+    const long long row = blockIdx.x;  // (seq, q head)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seq = int(row / num_q_heads);
     const int L = __ldg(context_lens + seq);
-    float* o = out + gw * D + lane * DPL;
+    float* o = out + row * D;
     if (L < 0 || L > max_context_len) {
-        if (lane == 0) set_error(err, ERR_BOUNDS);
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) o[e] = NAN;
+        if (threadIdx.x == 0) set_error(err, ERR_BOUNDS);
+        for (int d = threadIdx.x; d < D; d += NT) o[d] = NAN;
         return;
     }
     const int np = (L + partition_size - 1) / partition_size;
-    const size_t base = size_t(gw) * num_partitions;
+    if (np == 0) {
+        for (int d = threadIdx.x; d < D; d += NT) o[d] = 0.f;
+        return;
+    }
+    const size_t base = size_t(row) * num_partitions;
+
+    float M = -INFINITY;
+    for (int k = threadIdx.x; k < np; k += NT) M = fmaxf(M, tmp_m[base + k]);
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, s));
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < MERGE_WARPS; ++w) M = fmaxf(M, red[w]);
+    __syncthreads();
+    float W = 0.f;
+    for (int k = threadIdx.x; k < np; k += NT) W += tmp_l[base + k] * exp2_approx((tmp_m[base + k] - M) * kLog2e);
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) W += __shfl_xor_sync(FULL_MASK, W, s);
+    if (lane == 0) red[warp] = W;
+    __syncthreads();
+    W = 0.f;
+#pragma unroll
+    for (int w = 0; w < MERGE_WARPS; ++w) W += red[w];
+
     float acc[DPL];
 #pragma unroll
     for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-    if (np == 0) {
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) o[e] = 0.f;
-        return;
-    }
-    float M = -INFINITY;
-    for (int k = lane; k < np; k += 32) M = fmaxf(M, tmp_m[base + k]);
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, s));
-    float W = 0.f;
-    for (int k0 = 0; k0 < np; k0 += 32) {
-        const int k = k0 + lane;
-        const float wk = k < np ? tmp_l[base + k] * exp2_approx((tmp_m[base + k] - M) * kLog2e) : 0.f;
-        W += wk;
-        const int n = min(32, np - k0);
-        for (int j = 0; j < n; ++j) {
-            const float w = __shfl_sync(FULL_MASK, wk, j);
-            const float* src = tmp_out + (base + k0 + j) * D + lane * DPL;
-            if constexpr (DPL == 4) {
-                const float4 x = *reinterpret_cast<const float4*>(src);
-                acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
-            } else {
-                const float2 x = *reinterpret_cast<const float2*>(src);
-                acc[0] += w * x.x; acc[1] += w * x.y;
-            }
+#pragma unroll 4
+    for (int k = warp; k < np; k += MERGE_WARPS) {
+        const float w = tmp_l[base + k] * exp2_approx((tmp_m[base + k] - M) * kLog2e);
+        const float* src = tmp_out + (base + k) * D + lane * DPL;
+        if constexpr (DPL == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src);
+            acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+        } else {
+            const float2 x = *reinterpret_cast<const float2*>(src);
+            acc[0] += w * x.x; acc[1] += w * x.y;
         }
     }
 #pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) W += __shfl_xor_sync(FULL_MASK, W, s);
+    for (int e = 0; e < DPL; ++e) accs[warp][lane * DPL + e] = acc[e];
+    __syncthreads();
+    for (int d = threadIdx.x; d < D; d += NT) {
+        float s = 0.f;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) o[e] = acc[e] / W;
+        for (int w = 0; w < MERGE_WARPS; ++w) s += accs[w][d];
+        o[d] = s / W;
+    }
 }
 
 // ------------------------------------------------------ bounded-wait check
@@ -381,18 +403,19 @@ pf_status pf_paged_attention_merge(const void* workspace, const int32_t* context
     if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
     const int np = max_context_len > 0 ? int(((long long)max_context_len + partition_size - 1) / partition_size) : 1;
     const char* ws = static_cast<const char*>(workspace);
-    const long long warps = (long long)num_seqs * num_q_heads;
-    const unsigned blocks = unsigned((warps + 7) / 8);
+    const long long rows = (long long)num_seqs * num_q_heads;
+    if (rows > INT32_MAX) return PF_ERR_INVALID_ARG;
+    const unsigned blocks = unsigned(rows);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float* to = reinterpret_cast<const float*>(ws + off_o);
     const float* tm = reinterpret_cast<const float*>(ws + off_m);
     const float* tl = reinterpret_cast<const float*>(ws + off_l);
     if (head_dim == 64)
-        lse_merge_kernel<64><<<blocks, 256, 0, s>>>(to, tm, tl, context_lens, num_seqs, num_q_heads, partition_size,
-                                                    np, max_context_len, out, err);
+        lse_merge_kernel<64><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs, num_q_heads,
+                                                                 partition_size, np, max_context_len, out, err);
     else
-        lse_merge_kernel<128><<<blocks, 256, 0, s>>>(to, tm, tl, context_lens, num_seqs, num_q_heads,
-                                                     partition_size, np, max_context_len, out, err);
+        lse_merge_kernel<128><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs, num_q_heads,
+                                                                  partition_size, np, max_context_len, out, err);
     return cudaGetLastError() == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }
 

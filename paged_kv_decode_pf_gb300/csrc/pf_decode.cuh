@@ -63,12 +63,16 @@ struct DecodeGeometry {
     static_assert(CPL * LPT == CHUNKS_PER_ROW && NPASS * TPP == TT, "geometry");
 };
 
+// Bytes of the per-warp failure flags, padded so the mbarriers that follow stay aligned.
+template <int NW>
+constexpr int flag_bytes() { return (NW * 4 + 15) / 16 * 16; }
+
 template <int D, int G, int NW, int NST>
 constexpr size_t decode_smem_bytes() {
     using Geo = DecodeGeometry<D, G>;
     return size_t(NW) * NST * 2 * Geo::TILE_BYTES      // K/V stages
            + size_t(NW) * Geo::PSM_PAD * 4             // probabilities, alpha; then m, l
-           + 16                                        // per-warp failure flags (NW <= 4)
+           + flag_bytes<NW>()                          // per-warp failure flags
            + size_t(NW) * NST * 8;                     // mbarriers
 }
 
@@ -114,12 +118,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     constexpr int DUP = Geo::DUP, DPL = Geo::DPL, ROW = Geo::ROW_BYTES, TILE = Geo::TILE_BYTES;
     constexpr int PSM_PAD = Geo::PSM_PAD;
     constexpr int R = NST + 2;  // table entries lane 0 holds ahead of the copies
-    static_assert(NW <= 4, "flag area holds 4 warps");
 
     extern __shared__ __align__(128) unsigned char smem[];
     float* psm_all = reinterpret_cast<float*>(smem + size_t(NW) * NST * 2 * TILE);
     int* flags = reinterpret_cast<int*>(psm_all + NW * PSM_PAD);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(flags) + 16);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(flags) + flag_bytes<NW>());
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tp = lane / LPT, sl = lane % LPT;

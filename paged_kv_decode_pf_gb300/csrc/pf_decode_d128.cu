@@ -2,10 +2,18 @@
 // 4 warps per CTA, 3 stages of 16-token K+V tiles (8 KiB) per warp, two CTAs per SM.
 #include "pf_decode.cuh"
 
+// Warps per CTA and stages per warp (compile-time tunables).
+#ifndef PF_D128_WARPS
+#define PF_D128_WARPS 4
+#endif
+#ifndef PF_D128_STAGES
+#define PF_D128_STAGES 3
+#endif
+
 namespace pf {
 
 cudaError_t launch_decode_d128(const DecodeParams& p, int group, bool partition, cudaStream_t stream) {
-    return launch_decode_for_dim<128, 4, 3>(p, group, partition, stream);
+    return launch_decode_for_dim<128, PF_D128_WARPS, PF_D128_STAGES>(p, group, partition, stream);
 }
 
 }  // namespace pf
