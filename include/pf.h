@@ -189,6 +189,39 @@ PF_API const char* pf_status_string(pf_status status);
  */
 PF_API pf_status pf_debug_bounded_wait(int64_t limit_ns, pf_stream_t stream);
 
+/*
+ * Split-K decode that allocates nothing.  The paper has no counterpart; this
+ * exists for callers that cannot hand the library a workspace: a plugin or
+ * custom op inside a host runtime that owns all device memory and offers no
+ * allocator on the decode path, a decode loop that must not call cudaMalloc
+ * (it can synchronise the whole device and stall other streams), or a process
+ * whose memory is already fully reserved by another allocator.
+ *
+ * It computes the same result as pf_paged_attention_decode_partition followed
+ * by pf_paged_attention_merge (same arguments, same supported shapes), with
+ * the partials kept in a scratch array compiled into the library: a
+ * file-scope __device__ array of PF_SPLIT_NOALLOC_SCRATCH_BYTES bytes that a
+ * device keeps from the first use until the process exits.  When the workspace
+ * layout for these arguments (pf_paged_attention_partition_workspace_size) is
+ * larger than that, the call returns PF_ERR_UNSUPPORTED and launches nothing.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call outside any stream
+ * capture.  The call performs no allocation (no cudaMalloc, cudaFree or
+ * allocating library routine).  Every call on a device shares the one array
+ * and leaves its partials there; nothing in it has to start at zero, because
+ * the partition pass writes every partial the merge then reads.  Calls whose
+ * executions overlap on the GPU (for example on two streams of one device)
+ * race on the array and must be ordered by the caller.
+ */
+#define PF_SPLIT_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+PF_API pf_status pf_paged_attention_split_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                                  const int32_t* block_tables, const int32_t* context_lens,
+                                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                                  int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                                  float scale, int partition_size, int max_context_len,
+                                                  float* out, pf_stream_t stream);
+
 /* Library version, e.g. "0.1.0". */
 PF_API const char* pf_version(void);
 

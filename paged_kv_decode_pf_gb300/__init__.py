@@ -230,6 +230,37 @@ def paged_attention_split(q, k_cache, v_cache, block_tables, context_lens, parti
     return paged_attention_merge(workspace, context_lens, Hq, D, partition_size, max_context_len, out)
 
 
+SPLIT_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024   # PF_SPLIT_NOALLOC_SCRATCH_BYTES in pf.h
+
+
+def _split_noalloc_fn():
+    f = lib().pf_paged_attention_split_noalloc
+    if f.argtypes is None:
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        f.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, ctypes.c_float, i32, i32, P, P]
+        f.restype = ctypes.c_int
+    return f
+
+
+def paged_attention_split_noalloc(q, k_cache, v_cache, block_tables, context_lens, partition_size: int,
+                                  max_context_len: int, scale: Optional[float] = None,
+                                  out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Split-K decode whose partials live in the library's fixed scratch array instead of a
+    caller workspace, for callers that cannot allocate device memory on the decode path.
+    Calls that overlap on one device race on that array; `out` is still the caller's."""
+    S, Hq, Hkv, D, bs, NB, MB = _attn_shapes(q, k_cache, v_cache, block_tables, context_lens)
+    if out is None:
+        out = torch.empty((S, Hq, D), dtype=torch.float32, device=q.device)
+    _cuda(out, "out", (torch.float32,), 3)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        _check(_split_noalloc_fn()(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+                                   context_lens.data_ptr(), S, Hq, Hkv, D, bs, MB, NB, scale, partition_size,
+                                   max_context_len, out.data_ptr(), _stream(q.device)),
+               "pf_paged_attention_split_noalloc")
+    return out
+
+
 def get_device_error(device=None) -> int:
     """Synchronise the current stream, read and clear the device error word; returns the status code."""
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
