@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--workload", type=int, default=4, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-extras", action="store_true", help="skip the other named workloads")
     ap.add_argument("--oracle-seconds", type=float, default=15.0, help="CPU work of the oracle baseline sample")
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="profiling aid: keep only the first N sequences of the workload (0 = all)")
     ap.add_argument("--decode-variant", default="decode", choices=["decode", "split"],
                     help="headline path: single-pass decode or partition+merge")
     return ap.parse_args()
@@ -220,18 +222,45 @@ class Runner:
         return b
 
 
+def host_seconds_per_step(runner, flush=None, n=10):
+    """Host time to enqueue one step (the Python binding's argument checks and launches)."""
+    import torch
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(n):
+        runner.step()
+        if flush is not None:
+            flush.zero_()
+    host = (time.perf_counter() - t) / n
+    torch.cuda.synchronize()
+    return host
+
+
+def hold_gpu(seconds):
+    """Queue a spin kernel so that everything enqueued after it runs back to back on the
+    GPU, even when the host takes longer to enqueue a step than the GPU takes to run it."""
+    import torch
+    if seconds > 0:
+        torch.cuda._sleep(int(min(seconds, 2.0) * 2.2e9))
+
+
 def time_steps(runner, steps, warmup, flush=None, dist=None, sampler=None):
-    """(ms per step over the timed region, mean ms of the dominant kernel, per-launch ms list)."""
+    """(ms per step over the timed region, mean ms of the dominant kernel, per-launch ms list).
+
+    A spin kernel queued first covers the host's enqueue time of the whole loop, so
+    the events measure the GPU back to back rather than the host's launch rate."""
     import torch
     for _ in range(warmup):
         runner.step()
         if flush is not None:
             flush.zero_()
+    host = host_seconds_per_step(runner, flush)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
+    hold_gpu(1.5 * host * steps + 0.005)
     if sampler is not None:
         sampler.start()
     t0.record()
@@ -248,6 +277,21 @@ def time_steps(runner, steps, warmup, flush=None, dist=None, sampler=None):
     total = t0.elapsed_time(t1)
     per = [a.elapsed_time(b) for a, b in evs]
     return total / steps, statistics.fmean(per), per
+
+
+def max_over_ranks(value, dist, device):
+    """The largest `value` over all ranks (the slowest rank decides the job's time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, bytes_per_step_per_rank, ms_per_step):
+    """Whole-job GB/s: every rank processes its own batch (weak scaling) in the slowest rank's time."""
+    return world * bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
 def time_e2e(runner, steps, warmup):
@@ -342,7 +386,7 @@ def main():
     import paged_kv_decode_pf_gb300 as pf
     from workloads import CONFIGS, make_config
 
-    wl = make_config(args.workload)
+    wl = first_sequences(make_config(args.workload), args.seqs)
     runner = Runner(pf, wl, dev, args.decode_variant)
     flush = None
     if runner.step_bytes() < 2 * L2_BYTES:
@@ -355,12 +399,9 @@ def main():
     ms_step, ms_dom, per = time_steps(runner, args.steps, max(args.warmup, 3), flush, dist, sampler)
     pf.check_device_error()
     sampler.close()
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_step, dist, dev)
     step_bytes = runner.step_bytes()
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = job_throughput(world, step_bytes, ms_step)
     dom_bytes = runner.dominant_bytes()
     achieved = dom_bytes / (ms_dom * 1e-3) / 1e9
     e2e_ms, h2d, d2h = time_e2e(runner, min(args.steps, 500), 3)
@@ -443,6 +484,17 @@ def main():
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def first_sequences(wl, n):
+    """The workload restricted to its first n sequences (the whole pool stays)."""
+    import dataclasses
+    if n <= 0 or n >= wl.num_seqs:
+        return wl
+    sm = wl.slot_mapping[:n] if wl.slot_mapping is not None else None
+    return dataclasses.replace(wl, num_seqs=n, q=wl.q[:n], block_tables=wl.block_tables[:n],
+                               context_lens=wl.context_lens[:n], slot_mapping=sm,
+                               new_k=None if sm is None else wl.new_k[:n], new_v=None if sm is None else wl.new_v[:n])
 
 
 def runner_split(args, wl):

@@ -89,13 +89,15 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __r
 
 // ------------------------------------------------------------------- merge
 
-// One CTA of MERGE_WARPS warps per (sequence, query head): log-sum-exp merge of
-// its partitions.  The maximum and the weight sum are reduced over the whole
-// CTA; the warps then take every MERGE_WARPS-th partition (lanes own D/32
-// dims, four partitions in flight per warp) and add their sums in shared memory.
-constexpr int MERGE_WARPS = 4;
+// Log-sum-exp merge.  A CTA of 8 warps serves 8 / WPR rows (sequence, query
+// head); the WPR warps of a row each take every WPR-th partition, with lanes
+// owning D/32 dims and up to 8 partitions in flight per warp, and add their sums
+// in shared memory.  Every warp of a row first reduces the maximum m_k and the
+// weight sum over all partitions itself (lane-parallel), so no barrier is needed
+// before the accumulation.  WPR grows with the partition count (host side).
+constexpr int MERGE_WARPS = 8;
 
-template <int D>
+template <int D, int WPR>
 __global__ void __launch_bounds__(MERGE_WARPS * 32) lse_merge_kernel(const float* __restrict__ tmp_out,
                                                                      const float* __restrict__ tmp_m,
                                                                      const float* __restrict__ tmp_l,
@@ -105,70 +107,91 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) lse_merge_kernel(const float
                                                                      int max_context_len, float* __restrict__ out,
                                                                      unsigned* err) {
     constexpr int DPL = D / 32;
-    constexpr int NT = MERGE_WARPS * 32;
+    constexpr int ROWS = MERGE_WARPS / WPR;
     constexpr float kLog2e = 1.4426950408889634f;
-    __shared__ float red[MERGE_WARPS];
     __shared__ __align__(16) float accs[MERGE_WARPS][D];
-    const long long row = blockIdx.x;  // (seq, q head)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int seq = int(row / num_q_heads);
-    const int L = __ldg(context_lens + seq);
-    float* o = out + row * D;
-    if (L < 0 || L > max_context_len) {
-        if (threadIdx.x == 0) set_error(err, ERR_BOUNDS);
-        for (int d = threadIdx.x; d < D; d += NT) o[d] = NAN;
-        return;
-    }
-    const int np = (L + partition_size - 1) / partition_size;
-    if (np == 0) {
-        for (int d = threadIdx.x; d < D; d += NT) o[d] = 0.f;
-        return;
-    }
-    const size_t base = size_t(row) * num_partitions;
+    const int rloc = warp / WPR, sub = warp % WPR;
+    const long long row = (long long)blockIdx.x * ROWS + rloc;   // (seq, q head)
+    const bool active = row < (long long)num_seqs * num_q_heads;
+    const int L = active ? __ldg(context_lens + row / num_q_heads) : 0;
+    const bool bad = active && (L < 0 || L > max_context_len);
+    if (bad && sub == 0 && lane == 0) set_error(err, ERR_BOUNDS);
+    const int np = (active && !bad) ? (L + partition_size - 1) / partition_size : 0;
+    const size_t base = active ? size_t(row) * num_partitions : 0;
 
     float M = -INFINITY;
-    for (int k = threadIdx.x; k < np; k += NT) M = fmaxf(M, tmp_m[base + k]);
+    for (int k = lane; k < np; k += 32) M = fmaxf(M, tmp_m[base + k]);
 #pragma unroll
     for (int s = 16; s >= 1; s >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, s));
-    if (lane == 0) red[warp] = M;
-    __syncthreads();
-    M = red[0];
-#pragma unroll
-    for (int w = 1; w < MERGE_WARPS; ++w) M = fmaxf(M, red[w]);
-    __syncthreads();
     float W = 0.f;
-    for (int k = threadIdx.x; k < np; k += NT) W += tmp_l[base + k] * exp2_approx((tmp_m[base + k] - M) * kLog2e);
+    for (int k = lane; k < np; k += 32) W += tmp_l[base + k] * exp2_approx((tmp_m[base + k] - M) * kLog2e);
 #pragma unroll
     for (int s = 16; s >= 1; s >>= 1) W += __shfl_xor_sync(FULL_MASK, W, s);
-    if (lane == 0) red[warp] = W;
-    __syncthreads();
-    W = 0.f;
-#pragma unroll
-    for (int w = 0; w < MERGE_WARPS; ++w) W += red[w];
 
     float acc[DPL];
 #pragma unroll
     for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-#pragma unroll 4
-    for (int k = warp; k < np; k += MERGE_WARPS) {
-        const float w = tmp_l[base + k] * exp2_approx((tmp_m[base + k] - M) * kLog2e);
+    auto load_row = [&](int k, float (&x)[DPL]) {
         const float* src = tmp_out + (base + k) * D + lane * DPL;
         if constexpr (DPL == 4) {
-            const float4 x = *reinterpret_cast<const float4*>(src);
-            acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
         } else {
-            const float2 x = *reinterpret_cast<const float2*>(src);
-            acc[0] += w * x.x; acc[1] += w * x.y;
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            x[0] = v.x; x[1] = v.y;
         }
+    };
+    constexpr int BATCH = 8;  // partitions whose loads are in flight together
+    int k = sub;
+    for (; k + (BATCH - 1) * WPR < np; k += BATCH * WPR) {
+        float mk[BATCH], lk[BATCH], x[BATCH][DPL];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            mk[u] = tmp_m[base + k + u * WPR];
+            lk[u] = tmp_l[base + k + u * WPR];
+            load_row(k + u * WPR, x[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const float w = lk[u] * exp2_approx((mk[u] - M) * kLog2e);
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] += w * x[u][e];
+        }
+    }
+    for (; k < np; k += WPR) {
+        float x[DPL];
+        load_row(k, x);
+        const float w = tmp_l[base + k] * exp2_approx((tmp_m[base + k] - M) * kLog2e);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[e] += w * x[e];
     }
 #pragma unroll
     for (int e = 0; e < DPL; ++e) accs[warp][lane * DPL + e] = acc[e];
     __syncthreads();
-    for (int d = threadIdx.x; d < D; d += NT) {
+    if (!active) return;
+    float* o = out + row * D;
+    for (int d = sub * 32 + lane; d < D; d += WPR * 32) {
         float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < MERGE_WARPS; ++w) s += accs[w][d];
-        o[d] = s / W;
+        for (int j = 0; j < WPR; ++j) s += accs[rloc * WPR + j][d];
+        o[d] = bad ? NAN : (np == 0 ? 0.f : s / W);
+    }
+}
+
+template <int D>
+static void launch_merge(int wpr, unsigned blocks, cudaStream_t s, const float* to, const float* tm, const float* tl,
+                         const int32_t* context_lens, int num_seqs, int num_q_heads, int partition_size, int np,
+                         int max_context_len, float* out, unsigned* err) {
+    switch (wpr) {
+        case 1: lse_merge_kernel<D, 1><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs,
+                    num_q_heads, partition_size, np, max_context_len, out, err); break;
+        case 2: lse_merge_kernel<D, 2><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs,
+                    num_q_heads, partition_size, np, max_context_len, out, err); break;
+        case 4: lse_merge_kernel<D, 4><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs,
+                    num_q_heads, partition_size, np, max_context_len, out, err); break;
+        default: lse_merge_kernel<D, 8><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs,
+                    num_q_heads, partition_size, np, max_context_len, out, err); break;
     }
 }
 
@@ -323,6 +346,7 @@ pf_status pf_paged_attention_decode(const void* q, const void* k_cache, const vo
     if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
     DecodeParams p = make_params(a, err);
     p.out = out;
+    p.order_mode = (num_seqs > 1 && num_seqs <= kMaxSortedSeqsDecode) ? ORDER_SORTED : ORDER_NATURAL;
     const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, false,
                                         reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
@@ -382,6 +406,7 @@ pf_status pf_paged_attention_decode_partition(const void* q, const void* k_cache
     p.partition_size = partition_size;
     p.num_partitions = int(np);
     p.max_context_len = max_context_len;
+    p.order_mode = num_seqs <= kMaxSortedSeqsPartition ? ORDER_SORTED : ORDER_NATURAL;
     const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, true,
                                         reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
@@ -404,18 +429,20 @@ pf_status pf_paged_attention_merge(const void* workspace, const int32_t* context
     const int np = max_context_len > 0 ? int(((long long)max_context_len + partition_size - 1) / partition_size) : 1;
     const char* ws = static_cast<const char*>(workspace);
     const long long rows = (long long)num_seqs * num_q_heads;
-    if (rows > INT32_MAX) return PF_ERR_INVALID_ARG;
-    const unsigned blocks = unsigned(rows);
+    // warps per row: enough that each warp has about 16 partitions or fewer to add
+    const int wpr = np >= 128 ? 8 : np >= 64 ? 4 : np >= 32 ? 2 : 1;
+    const long long blocks = (rows + (MERGE_WARPS / wpr) - 1) / (MERGE_WARPS / wpr);
+    if (blocks > INT32_MAX) return PF_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float* to = reinterpret_cast<const float*>(ws + off_o);
     const float* tm = reinterpret_cast<const float*>(ws + off_m);
     const float* tl = reinterpret_cast<const float*>(ws + off_l);
     if (head_dim == 64)
-        lse_merge_kernel<64><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs, num_q_heads,
-                                                                 partition_size, np, max_context_len, out, err);
+        launch_merge<64>(wpr, unsigned(blocks), s, to, tm, tl, context_lens, num_seqs, num_q_heads, partition_size,
+                         np, max_context_len, out, err);
     else
-        lse_merge_kernel<128><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs, num_q_heads,
-                                                                  partition_size, np, max_context_len, out, err);
+        launch_merge<128>(wpr, unsigned(blocks), s, to, tm, tl, context_lens, num_seqs, num_q_heads, partition_size,
+                          np, max_context_len, out, err);
     return cudaGetLastError() == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }
 

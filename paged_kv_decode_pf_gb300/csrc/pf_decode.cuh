@@ -67,13 +67,100 @@ struct DecodeGeometry {
 template <int NW>
 constexpr int flag_bytes() { return (NW * 4 + 15) / 16 * 16; }
 
+// Offset, from the first mbarrier, of the int array used to order work items.
+template <int NW, int NST>
+constexpr int sorted_keys_offset() { return (NW * NST * 8 + 15) / 16 * 16; }
+
 template <int D, int G, int NW, int NST>
 constexpr size_t decode_smem_bytes() {
     using Geo = DecodeGeometry<D, G>;
     return size_t(NW) * NST * 2 * Geo::TILE_BYTES      // K/V stages
            + size_t(NW) * Geo::PSM_PAD * 4             // probabilities, alpha; then m, l
            + flag_bytes<NW>()                          // per-warp failure flags
-           + size_t(NW) * NST * 8;                     // mbarriers
+           + sorted_keys_offset<NW, NST>();            // mbarriers (+ padding)
+    // followed, in ORDER_SORTED launches, by round_up(num_seqs, 4) ints of keys
+}
+
+// ORDER_SORTED item selection (see pf_internal.h).  `keys` holds round_up(S, 4)
+// ints of shared memory.  Returns false when this CTA has no item.
+template <int NW, bool PART>
+__device__ __forceinline__ bool select_sorted_item(const DecodeParams& p, int* keys, int* seq, int* kvh,
+                                                   int* part) {
+    __shared__ int s_item;
+    __shared__ int s_warp_sum[NW];
+    constexpr int NT = NW * 32;
+    const int S = p.num_seqs;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    *kvh = blockIdx.x % p.num_kv_heads;
+    const int r = blockIdx.x / p.num_kv_heads;
+    if constexpr (!PART) {
+        // key = (length, reversed index): unique, so the ranks are a permutation
+        const int Sp = (S + 3) & ~3;
+        for (int i = tid; i < Sp; i += NT) {
+            int key = -1;
+            if (i < S) {
+                const int Li = min(max(__ldg(p.context_lens + i), 0), (1 << 20) - 1);
+                key = (Li << 10) | (1023 - i);
+            }
+            keys[i] = key;
+        }
+        __syncthreads();
+        for (int i = tid; i < S; i += NT) {
+            const int ki = keys[i];
+            int rank = 0;
+            for (int j = 0; j < Sp; j += 4) {
+                const int4 kj = *reinterpret_cast<const int4*>(keys + j);
+                rank += int(kj.x > ki) + int(kj.y > ki) + int(kj.z > ki) + int(kj.w > ki);
+            }
+            if (rank == r) s_item = i;
+        }
+        __syncthreads();
+        *seq = s_item;
+        *part = 0;
+        return true;
+    } else {
+        // non-empty partitions per sequence, then an inclusive prefix over sequences
+        const int P = p.partition_size;
+        bool bad = false;
+        for (int i = tid; i < S; i += NT) {
+            const int Li = __ldg(p.context_lens + i);
+            const bool b = Li < 0 || Li > p.max_context_len;
+            bad = bad || b;
+            keys[i] = b ? 0 : (Li + P - 1) / P;
+        }
+        if (bad && blockIdx.x == 0) set_error(p.err, ERR_BOUNDS);  // the merge NaN-fills those rows
+        __syncthreads();
+        const int per = (S + NT - 1) / NT;
+        const int i0 = tid * per;
+        int sum = 0;
+        for (int k = 0; k < per; ++k)
+            if (i0 + k < S) sum += keys[i0 + k];
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL_MASK, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_warp_sum[warp] = incl;
+        __syncthreads();
+        int run = incl - sum;
+        for (int w = 0; w < warp; ++w) run += s_warp_sum[w];
+        for (int k = 0; k < per; ++k)
+            if (i0 + k < S) {
+                run += keys[i0 + k];
+                keys[i0 + k] = run;
+            }
+        __syncthreads();
+        if (r >= keys[S - 1]) return false;
+        int lo = 0, hi = S - 1;  // first sequence whose inclusive prefix exceeds r
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (keys[mid] > r) hi = mid; else lo = mid + 1;
+        }
+        *seq = lo;
+        *part = r - (lo > 0 ? keys[lo - 1] : 0);
+        return true;
+    }
 }
 
 // Sum of v[0..G-1] over the LPT lanes of one token, spread so that afterwards
@@ -132,7 +219,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
 
     // ---- which item
     int seq, kvh, part = 0;
-    if constexpr (PART) {
+    if (p.order_mode == ORDER_SORTED) {
+        int* keys = reinterpret_cast<int*>(bars + sorted_keys_offset<NW, NST>() / 8);
+        if (!select_sorted_item<NW, PART>(p, keys, &seq, &kvh, &part)) return;
+    } else if constexpr (PART) {
         part = blockIdx.x % p.num_partitions;
         const int rest = blockIdx.x / p.num_partitions;
         kvh = rest % p.num_kv_heads;
@@ -420,7 +510,9 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
 
 template <int D, int G, int NW, int NST, bool PART>
 cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream) {
-    constexpr size_t smem = decode_smem_bytes<D, G, NW, NST>();
+    constexpr size_t smem_base = decode_smem_bytes<D, G, NW, NST>();
+    constexpr size_t smem_max = smem_base + size_t(kMaxSortedSeqsPartition) * 4;
+    const size_t smem = smem_base + (p.order_mode == ORDER_SORTED ? size_t((p.num_seqs + 3) & ~3) * 4 : 0);
     auto kern = paged_decode_kernel<D, G, NW, NST, PART>;
     static std::atomic<unsigned long long> configured{0};  // one bit per device ordinal
     int dev = 0;
@@ -428,7 +520,7 @@ cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
     if (bit == 0 || !(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_max));
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }

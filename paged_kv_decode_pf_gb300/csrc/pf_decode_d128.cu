@@ -1,5 +1,5 @@
 // head_dim = 128 instantiations of the decode / partition kernel:
-// 4 warps per CTA, 3 stages of 16-token K+V tiles (8 KiB) per warp, two CTAs per SM.
+// 4 warps per CTA, 2 stages of 16-token K+V tiles (8 KiB) per warp, three CTAs per SM.
 #include "pf_decode.cuh"
 
 // Warps per CTA and stages per warp (compile-time tunables).
@@ -7,7 +7,7 @@
 #define PF_D128_WARPS 4
 #endif
 #ifndef PF_D128_STAGES
-#define PF_D128_STAGES 3
+#define PF_D128_STAGES 2
 #endif
 
 namespace pf {

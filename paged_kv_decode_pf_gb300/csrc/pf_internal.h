@@ -34,7 +34,21 @@ struct DecodeParams {
     int partition_size;      // partition pass: tokens per partition (multiple of 16)
     int num_partitions;      // partition pass: NP
     int max_context_len;     // partition pass: bound every context length must respect
+    int order_mode;          // ORDER_NATURAL or ORDER_SORTED (see below)
 };
+
+// How CTAs map to work items.
+//  ORDER_NATURAL: CTA b serves (sequence b / Hkv, kv head b % Hkv); partition pass:
+//                 b -> (partition, kv head, sequence), empty partitions exit at once.
+//  ORDER_SORTED:  decode: CTA b serves the sequence of rank b / Hkv when sequences
+//                 are ordered longest first (ties by index), so that the hardware's
+//                 in-order CTA dispatch approximates longest-processing-time-first
+//                 scheduling; partition pass: CTA b serves the (b / Hkv)-th non-empty
+//                 (sequence, partition) pair, so the empty ones form the grid's tail.
+constexpr int ORDER_NATURAL = 0;
+constexpr int ORDER_SORTED = 1;
+constexpr int kMaxSortedSeqsDecode = 512;      // ranking costs O(S^2 / threads) per CTA
+constexpr int kMaxSortedSeqsPartition = 1024;  // the prefix scan costs O(S / threads)
 
 // Launch the single-pass decode kernel (partition == false) or the partition
 // pass (partition == true) for one head_dim.  Returns cudaSuccess or the launch error.
