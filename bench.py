@@ -487,13 +487,28 @@ def main():
 
 
 def first_sequences(wl, n):
-    """The workload restricted to its first n sequences (the whole pool stays)."""
+    """The workload restricted to its first n sequences, with the pool compacted to the
+    blocks they use (kept in pool order) and the tables and slots renumbered."""
     import dataclasses
     if n <= 0 or n >= wl.num_seqs:
         return wl
-    sm = wl.slot_mapping[:n] if wl.slot_mapping is not None else None
-    return dataclasses.replace(wl, num_seqs=n, q=wl.q[:n], block_tables=wl.block_tables[:n],
-                               context_lens=wl.context_lens[:n], slot_mapping=sm,
+    L = wl.context_lens[:n].astype(np.int64)
+    nblk = (L + wl.block_size - 1) // wl.block_size
+    tables = wl.block_tables[:n].copy()
+    used = np.unique(np.concatenate([tables[i, :nblk[i]] for i in range(n)]))
+    remap = np.full(wl.num_blocks, -1, dtype=np.int64)
+    remap[used] = np.arange(used.size)
+    for i in range(n):
+        tables[i, :nblk[i]] = remap[tables[i, :nblk[i]]]
+    sm = None
+    if wl.slot_mapping is not None:
+        s = wl.slot_mapping[:n].copy()
+        ok = s >= 0
+        s[ok] = remap[s[ok] // wl.block_size] * wl.block_size + s[ok] % wl.block_size
+        sm = s
+    return dataclasses.replace(wl, num_seqs=n, num_blocks=int(used.size), q=wl.q[:n], block_tables=tables,
+                               context_lens=wl.context_lens[:n], k_cache=np.ascontiguousarray(wl.k_cache[used]),
+                               v_cache=np.ascontiguousarray(wl.v_cache[used]), slot_mapping=sm,
                                new_k=None if sm is None else wl.new_k[:n], new_v=None if sm is None else wl.new_v[:n])
 
 
