@@ -188,12 +188,21 @@ class Runner:
             self.P = wl.partition_size or 512
             self.max_ctx = wl.max_context_len
             self.ws = pf.alloc_workspace(wl.num_seqs, wl.num_q_heads, wl.head_dim, self.max_ctx, self.P, dev)
-        self.kernels_per_step = (1 if self.append else 0) + (2 if self.split else 1)
-        self.dominant = "partition" if self.split else "decode"
+        self.fused = self.append and not self.split and variant == "fused"
+        self.kernels_per_step = 1 if self.fused else (1 if self.append else 0) + (2 if self.split else 1)
+        self.dominant = "partition" if self.split else ("decode_append" if self.fused else "decode")
 
     def step(self, ev=None):
         """One pass; when `ev` is a pair of CUDA events they bracket the dominant kernel."""
         pf = self.pf
+        if self.fused:   # append and attend in one launch
+            if ev is not None:
+                ev[0].record()
+            pf.paged_attention_decode_append(self.q, self.nk, self.nv, self.sm, self.kc, self.vc, self.bt, self.cl,
+                                             self.wl.scale, self.out)
+            if ev is not None:
+                ev[1].record()
+            return
         if self.append:
             pf.reshape_and_cache(self.nk, self.nv, self.sm, self.kc, self.vc)
         if ev is not None:
@@ -292,6 +301,32 @@ def max_over_ranks(value, dist, device):
 def job_throughput(world, bytes_per_step_per_rank, ms_per_step):
     """Whole-job GB/s: every rank processes its own batch (weak scaling) in the slowest rank's time."""
     return world * bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
+class CopyRunner:
+    """pf_copy_blocks over `pairs` random (src, dst) pairs of Llama-3-8B-shaped blocks
+    (8 kv heads x 16 tokens x 128 dims, bf16): a pure read + write stream."""
+
+    def __init__(self, pf, dev, pairs=4096, num_blocks=8192, shape=(8, 16, 128)):
+        import torch
+        self.pf = pf
+        g = torch.Generator(device=dev).manual_seed(11)
+        self.kc = torch.empty((num_blocks,) + shape, dtype=torch.bfloat16, device=dev)
+        self.vc = torch.empty_like(self.kc)
+        perm = torch.randperm(num_blocks, device=dev, generator=g)
+        self.mapping = torch.stack([perm[:pairs], perm[pairs:2 * pairs]], dim=1).contiguous()
+        self.pairs = pairs
+        self.block_bytes = int(np.prod(shape)) * 2
+
+    def step(self, ev=None):
+        if ev is not None:
+            ev[0].record()
+        self.pf.copy_blocks(self.kc, self.vc, self.mapping)
+        if ev is not None:
+            ev[1].record()
+
+    def step_bytes(self):
+        return self.pairs * 2 * self.block_bytes * 2      # K and V, read and written
 
 
 def time_e2e(runner, steps, warmup):
@@ -412,20 +447,21 @@ def main():
     if not args.no_extras and rank == 0:
         del runner
         torch.cuda.empty_cache()
-        for idx in [1, 2, 3, 5]:
-            if idx == args.workload:
+        for idx, variant in [(1, "decode"), (2, "decode"), (3, "decode"), (3, "fused"), (5, "decode")]:
+            if idx == args.workload and variant == "decode":
                 continue
             w = make_config(idx)
-            r = Runner(pf, w, dev)
+            r = Runner(pf, w, dev, variant)
             fl = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if r.step_bytes() < 2 * L2_BYTES \
                 else None
             n = 200 if fl is None else 400
             ms_s, ms_d, _ = time_steps(r, n, 10, fl)
             pf.check_device_error()
             b = r.step_bytes()
-            extras[CONFIGS[idx].name] = {
+            extras[CONFIGS[idx].name + ("_fused" if r.fused else "")] = {
                 "description": CONFIGS[idx].description,
-                "step": ("append + " if r.append else "") + ("partition + merge" if r.split else "decode"),
+                "step": "append and decode fused in one launch" if r.fused else
+                        ("append + " if r.append else "") + ("partition + merge" if r.split else "decode"),
                 "us_per_step": round(ms_s * 1e3, 2) if fl is None else None,
                 "us_dominant_kernel": round(ms_d * 1e3, 2),
                 "algorithmic_bytes": b,
@@ -437,6 +473,20 @@ def main():
             }
             del r, fl
             torch.cuda.empty_cache()
+        cr = CopyRunner(pf, dev)
+        ms_s, ms_d, _ = time_steps(cr, 200, 10)
+        pf.check_device_error()
+        cb = cr.step_bytes()
+        extras["copy_blocks"] = {
+            "description": "pf_copy_blocks: 4096 (src, dst) pairs of 8x16x128 bf16 blocks, K and V "
+                           "(268 MB read + 268 MB written)",
+            "step": "copy_blocks", "us_dominant_kernel": round(ms_d * 1e3, 2), "algorithmic_bytes": cb,
+            "gbs_dominant_kernel": round(cb / (ms_d * 1e-3) / 1e9, 1),
+            "frac_of_measured_copy_peak": round(cb / (ms_d * 1e-3) / 1e9 / peak, 3),
+            "l2": "inputs larger than L2",
+        }
+        del cr
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0:

@@ -96,6 +96,27 @@ PF_API pf_status pf_reshape_and_cache(const void* k, const void* v, const int64_
                                int64_t num_blocks, pf_stream_t stream);
 
 /*
+ * Block copy for the allocator: when a request forks (beam search, parallel
+ * sampling, a shared prompt whose last block is still being filled) it gets its
+ * own copy of a shared physical block before either side appends to it -- the
+ * device half of "physical KV blocks with logical per-request block tables ...
+ * reclamation" (ForgeLLM README, feature list).
+ *
+ *   for every pair j < num_pairs, with (src, dst) = (block_mapping[2j], block_mapping[2j+1]):
+ *     k_cache[dst][:][:][:] = k_cache[src][:][:][:];  v_cache likewise
+ *
+ * block_mapping is int64 [num_pairs][2] in device memory.  Bit-exact copy of
+ * whole blocks (every kv head and offset).  Destinations must be distinct and
+ * no destination may also be a source in the same call (the result is
+ * unspecified otherwise); src == dst is a no-op.  A pair with an id outside
+ * [0, num_blocks) is skipped and flags PF_ERR_DEVICE_BOUNDS.  head_dim must be
+ * a multiple of 8.  num_pairs == 0 launches nothing.
+ */
+PF_API pf_status pf_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, int64_t num_pairs,
+                                int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                pf_stream_t stream);
+
+/*
  * Decode attention over the paged cache, one query token per sequence, in a
  * single pass (ForgeLLM README, feature list: decode-only block-table attention
  * with online softmax, grouped-query heads):
@@ -116,6 +137,33 @@ PF_API pf_status pf_paged_attention_decode(const void* q, const void* k_cache, c
                                     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                     int block_size, int max_blocks_per_seq, int64_t num_blocks,
                                     float scale, float* out, pf_stream_t stream);
+
+/*
+ * One decode step in one launch: append each sequence's new token, then attend
+ * over the cache that includes it (the write and the read sides of "physical KV
+ * blocks with logical per-request block tables" and "decode-only block-table
+ * attention", ForgeLLM README, feature list, fused).  The result -- the caches
+ * after the call and out -- is that of
+ *     pf_reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, num_seqs, ...)
+ *     pf_paged_attention_decode(q, k_cache, v_cache, ...)
+ * for the decode case in which token i is the newest token of sequence i:
+ * slot_mapping[i] is -1 (sequence i appends nothing; it attends over its
+ * context_lens[i] cached tokens) or the slot of its position context_lens[i]-1,
+ * block_tables[i][(L-1)/bs]*bs + (L-1)%bs.  Any other slot flags
+ * PF_ERR_DEVICE_BOUNDS, writes nothing for that sequence and NaN-fills its rows.
+ * The new token's K/V enter the attention from k_new / v_new directly, so the
+ * slot's previous contents are never read.
+ *
+ *   k_new, v_new   [num_seqs, num_kv_heads, head_dim] bf16, 16-byte aligned
+ *   slot_mapping   [num_seqs] int64, 8-byte aligned
+ * Other arguments, shapes and errors as pf_paged_attention_decode.
+ */
+PF_API pf_status pf_paged_attention_decode_append(const void* q, const void* k_new, const void* v_new,
+                                                  const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                                  const int32_t* block_tables, const int32_t* context_lens,
+                                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                                  int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                                  float scale, float* out, pf_stream_t stream);
 
 /*
  * Split over context partitions ("flash-decoding") for long contexts.

@@ -68,6 +68,8 @@ def _bind(lib):
     lib.oracle_merge.restype = None
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i32
+    lib.oracle_copy_blocks.argtypes = [P, P, P, i64, i32, i32, i32, i64]
+    lib.oracle_copy_blocks.restype = i64
     return lib
 
 
@@ -105,6 +107,15 @@ class Oracle:
         s, sp = _c(slot_mapping, np.int64)
         bad = self.lib.oracle_reshape_and_cache(kp, vp, sp, kc.ctypes.data, vc.ctypes.data, T, Hkv, D,
                                                 block_size, NB)
+        return kc, vc, int(bad)
+
+    def copy_blocks(self, k_cache, v_cache, block_mapping):
+        """Returns new (k_cache, v_cache) after copying block_mapping[j] = (src, dst) pairs, and the
+        count of pairs skipped for an out-of-range id."""
+        NB, Hkv, bs, D = k_cache.shape
+        kc, vc = np.array(k_cache, dtype=np.uint16, copy=True), np.array(v_cache, dtype=np.uint16, copy=True)
+        bm, bp = _c(np.asarray(block_mapping).reshape(-1, 2), np.int64)
+        bad = self.lib.oracle_copy_blocks(kc.ctypes.data, vc.ctypes.data, bp, bm.shape[0], Hkv, D, bs, NB)
         return kc, vc, int(bad)
 
     def paged_attention(self, q, k_cache, v_cache, block_tables, context_lens, scale, threads: int = 0):

@@ -82,6 +82,30 @@ int64_t oracle_reshape_and_cache(const uint16_t* k, const uint16_t* v, const int
     return bad;
 }
 
+/* ------------------------------------------------------------- block copy */
+
+/* Copies whole physical blocks (every kv head, every offset) of both caches:
+ * for pair j, block block_mapping[2j] -> block block_mapping[2j+1].  This is the
+ * device side of giving a forked request its own copy of a shared block, on top
+ * of "physical KV blocks with logical per-request block tables" (ForgeLLM README,
+ * feature list).  Pairs with an id outside [0, num_blocks) are skipped and
+ * counted (the return value). */
+int64_t oracle_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, const int64_t* block_mapping,
+                           int64_t num_pairs, int num_kv_heads, int head_dim, int block_size,
+                           int64_t num_blocks) {
+    int64_t bad = 0;
+    const size_t per_block = (size_t)num_kv_heads * block_size * head_dim;
+    for (int64_t j = 0; j < num_pairs; ++j) {
+        int64_t src = block_mapping[2 * j], dst = block_mapping[2 * j + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) { ++bad; continue; }
+        for (size_t e = 0; e < per_block; ++e) {
+            k_cache[(size_t)dst * per_block + e] = k_cache[(size_t)src * per_block + e];
+            v_cache[(size_t)dst * per_block + e] = v_cache[(size_t)src * per_block + e];
+        }
+    }
+    return bad;
+}
+
 /* ----------------------------------------------------- one (seq, head) pair */
 
 typedef struct {

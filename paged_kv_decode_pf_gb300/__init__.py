@@ -73,6 +73,11 @@ def lib() -> ctypes.CDLL:
         L.pf_debug_bounded_wait.restype = st
         L.pf_version.argtypes = []
         L.pf_version.restype = ctypes.c_char_p
+        L.pf_copy_blocks.argtypes = [P, P, P, i64, i32, i32, i32, i64, P]
+        L.pf_copy_blocks.restype = st
+        L.pf_paged_attention_decode_append.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
+                                                       f32, P, P]
+        L.pf_paged_attention_decode_append.restype = st
         _LIB = L
     return _LIB
 
@@ -124,6 +129,20 @@ def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tens
                "pf_reshape_and_cache")
 
 
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: torch.Tensor) -> None:
+    """Copy whole physical blocks: block_mapping [n, 2] int64 of (src, dst) pairs."""
+    _cuda(k_cache, "k_cache", _BF16, 4)
+    _cuda(v_cache, "v_cache", _BF16, 4)
+    _cuda(block_mapping, "block_mapping", (torch.int64,), 2)
+    if v_cache.shape != k_cache.shape or block_mapping.shape[1] != 2:
+        raise ValueError("copy_blocks: inconsistent shapes")
+    NB, Hkv, bs, D = k_cache.shape
+    with torch.cuda.device(k_cache.device):
+        _check(lib().pf_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), block_mapping.data_ptr(),
+                                    block_mapping.shape[0], Hkv, D, bs, NB, _stream(k_cache.device)),
+               "pf_copy_blocks")
+
+
 def _attn_shapes(q, k_cache, v_cache, block_tables, context_lens):
     _cuda(q, "q", _BF16, 3)
     _cuda(k_cache, "k_cache", _BF16, 4)
@@ -151,6 +170,30 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                                                block_tables.data_ptr(), context_lens.data_ptr(), S, Hq, Hkv, D, bs,
                                                MB, NB, scale, out.data_ptr(), _stream(q.device)),
                "pf_paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                  slot_mapping: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                  scale: Optional[float] = None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode step in one launch: write k_new/v_new [S, Hkv, D] of each sequence's newest token to
+    slot_mapping [S] (int64; -1 = nothing to append), then attend.  Returns out [S, Hq, D] fp32."""
+    S, Hq, Hkv, D, bs, NB, MB = _attn_shapes(q, k_cache, v_cache, block_tables, context_lens)
+    _cuda(k_new, "k_new", _BF16, 3)
+    _cuda(v_new, "v_new", _BF16, 3)
+    _cuda(slot_mapping, "slot_mapping", (torch.int64,), 1)
+    if k_new.shape != (S, Hkv, D) or v_new.shape != k_new.shape or slot_mapping.shape[0] != S:
+        raise ValueError("paged_attention_decode_append: inconsistent shapes")
+    if out is None:
+        out = torch.empty((S, Hq, D), dtype=torch.float32, device=q.device)
+    _cuda(out, "out", (torch.float32,), 3)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        _check(lib().pf_paged_attention_decode_append(
+            q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), k_cache.data_ptr(),
+            v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), S, Hq, Hkv, D, bs, MB, NB, scale,
+            out.data_ptr(), _stream(q.device)), "pf_paged_attention_decode_append")
     return out
 
 
@@ -279,7 +322,7 @@ def debug_bounded_wait(limit_ns: int, device=None) -> None:
         _check(lib().pf_debug_bounded_wait(int(limit_ns), _stream(device)), "pf_debug_bounded_wait")
 
 
-__all__ = ["PFError", "lib", "version", "reshape_and_cache", "paged_attention_decode", "partition_workspace_layout",
+__all__ = ["PFError", "lib", "version", "reshape_and_cache", "copy_blocks", "paged_attention_decode", "partition_workspace_layout",
            "alloc_workspace", "workspace_views", "paged_attention_decode_partition", "paged_attention_merge",
            "paged_attention_split", "get_device_error", "check_device_error", "debug_bounded_wait",
            "num_partitions", "STATUS_NAMES"]

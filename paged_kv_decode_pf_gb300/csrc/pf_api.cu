@@ -28,7 +28,7 @@ static cudaError_t current_device(int* dev) {
 }
 
 // Device address of the error word of the current device, looked up once per device.
-static cudaError_t error_word(unsigned** out) {
+cudaError_t error_word(unsigned** out) {
     int dev = 0;
     cudaError_t e = current_device(&dev);
     if (e != cudaSuccess) return e;
@@ -42,7 +42,7 @@ static cudaError_t error_word(unsigned** out) {
     return cudaSuccess;
 }
 
-static cudaError_t sm_count(int* out) {
+cudaError_t sm_count(int* out) {
     int dev = 0;
     cudaError_t e = current_device(&dev);
     if (e != cudaSuccess) return e;
@@ -274,10 +274,8 @@ static DecodeParams make_params(const AttnArgs& a, unsigned* err) {
     return p;
 }
 
-static cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool partition,
-                                 cudaStream_t stream) {
-    return head_dim == 64 ? launch_decode_d64(p, group, partition, stream)
-                          : launch_decode_d128(p, group, partition, stream);
+static cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int mode, cudaStream_t stream) {
+    return head_dim == 64 ? launch_decode_d64(p, group, mode, stream) : launch_decode_d128(p, group, mode, stream);
 }
 
 }  // namespace pf
@@ -347,7 +345,35 @@ pf_status pf_paged_attention_decode(const void* q, const void* k_cache, const vo
     DecodeParams p = make_params(a, err);
     p.out = out;
     p.order_mode = (num_seqs > 1 && num_seqs <= kMaxSortedSeqsDecode) ? ORDER_SORTED : ORDER_NATURAL;
-    const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, false,
+    const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, MODE_DECODE,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
+}
+
+pf_status pf_paged_attention_decode_append(const void* q, const void* k_new, const void* v_new,
+                                           const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                           const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                           int max_blocks_per_seq, int64_t num_blocks, float scale, float* out,
+                                           pf_stream_t stream) {
+    const AttnArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, max_blocks_per_seq, num_blocks, scale};
+    pf_status st = check_attention(a);
+    if (st != PF_OK) return st;
+    if (num_seqs == 0) return PF_OK;
+    if (!aligned(out, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8))
+        return PF_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
+    DecodeParams p = make_params(a, err);
+    p.out = out;
+    p.order_mode = (num_seqs > 1 && num_seqs <= kMaxSortedSeqsDecode) ? ORDER_SORTED : ORDER_NATURAL;
+    p.k_new = static_cast<const uint16_t*>(k_new);
+    p.v_new = static_cast<const uint16_t*>(v_new);
+    p.slot_mapping = slot_mapping;
+    p.k_cache_w = static_cast<uint16_t*>(k_cache);
+    p.v_cache_w = static_cast<uint16_t*>(v_cache);
+    const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, MODE_DECODE_APPEND,
                                         reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }
@@ -407,7 +433,7 @@ pf_status pf_paged_attention_decode_partition(const void* q, const void* k_cache
     p.num_partitions = int(np);
     p.max_context_len = max_context_len;
     p.order_mode = num_seqs <= kMaxSortedSeqsPartition ? ORDER_SORTED : ORDER_NATURAL;
-    const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, true,
+    const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, MODE_PARTITION,
                                         reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }

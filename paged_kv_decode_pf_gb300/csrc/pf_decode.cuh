@@ -198,8 +198,10 @@ __device__ __forceinline__ void load_probs(const float* src, float (&pw)[G]) {
     }
 }
 
-template <int D, int G, int NW, int NST, bool PART>
+template <int D, int G, int NW, int NST, int MODE>
 __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParams p) {
+    constexpr bool PART = MODE == MODE_PARTITION;
+    constexpr bool APPEND = MODE == MODE_DECODE_APPEND;
     using Geo = DecodeGeometry<D, G>;
     constexpr int TT = Geo::TT, LPT = Geo::LPT, TPP = Geo::TPP, NPASS = Geo::NPASS, CPL = Geo::CPL;
     constexpr int DUP = Geo::DUP, DPL = Geo::DPL, ROW = Geo::ROW_BYTES, TILE = Geo::TILE_BYTES;
@@ -241,6 +243,23 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         t0 = part * p.partition_size;
         if (!len_bad && t0 >= L) return;  // empty partition: the merge never reads it
         t1 = min(L, t0 + p.partition_size);
+    }
+    // Decode with append: the new token of this sequence is its position L-1, and its
+    // slot must be that position's slot (or -1: nothing to append).  app_row is the
+    // token's row in the cache, [block][kv head][offset], or -1.
+    long long app_row = -1;
+    if constexpr (APPEND) {
+        const long long slot = __ldg(p.slot_mapping + seq);
+        if (!len_bad && slot != -1) {
+            bool ok = L >= 1;
+            if (ok) {
+                const int blk = __ldg(p.block_tables + size_t(seq) * p.max_blocks_per_seq + (L - 1) / p.block_size);
+                ok = blk >= 0 && (long long)blk < p.num_blocks &&
+                     slot == (long long)blk * p.block_size + (L - 1) % p.block_size;
+            }
+            if (ok) app_row = ((slot / p.block_size) * p.num_kv_heads + kvh) * p.block_size + slot % p.block_size;
+            else len_bad = true;  // nothing is written for this sequence
+        }
     }
     if (len_bad) {
         if (threadIdx.x == 0) set_error(p.err, ERR_BOUNDS);
@@ -352,6 +371,33 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         const unsigned char* Ks = my_stages + size_t(s) * 2 * TILE;
         const unsigned char* Vs = Ks + TILE;
         const int nvalid = min(TT, t1 - tile_token(k));
+        if constexpr (APPEND) {
+            const int r = (L - 1) - tile_token(k);
+            if (app_row >= 0 && r >= 0 && r < TT) {
+                // The tile holding the new token: its copy brought the slot's old bytes.
+                // Put the new K/V row in their place, and write it to the cache.
+                constexpr int LB = ROW / 32;  // bytes of the row per lane
+                const size_t src = (size_t(seq) * p.num_kv_heads + kvh) * D + lane * (LB / 2);
+                const size_t dst = size_t(app_row) * D + lane * (LB / 2);
+                unsigned char* kr = my_stages + size_t(s) * 2 * TILE + r * ROW + lane * LB;
+                if constexpr (LB == 8) {
+                    const uint2 kv = __ldg(reinterpret_cast<const uint2*>(p.k_new + src));
+                    const uint2 vv = __ldg(reinterpret_cast<const uint2*>(p.v_new + src));
+                    *reinterpret_cast<uint2*>(kr) = kv;
+                    *reinterpret_cast<uint2*>(kr + TILE) = vv;
+                    *reinterpret_cast<uint2*>(p.k_cache_w + dst) = kv;
+                    *reinterpret_cast<uint2*>(p.v_cache_w + dst) = vv;
+                } else {
+                    const uint32_t kv = __ldg(reinterpret_cast<const uint32_t*>(p.k_new + src));
+                    const uint32_t vv = __ldg(reinterpret_cast<const uint32_t*>(p.v_new + src));
+                    *reinterpret_cast<uint32_t*>(kr) = kv;
+                    *reinterpret_cast<uint32_t*>(kr + TILE) = vv;
+                    *reinterpret_cast<uint32_t*>(p.k_cache_w + dst) = kv;
+                    *reinterpret_cast<uint32_t*>(p.v_cache_w + dst) = vv;
+                }
+                __syncwarp();
+            }
+        }
 
         // -- scores of this lane's tokens for head hh, base-2 units
         float sc[NPASS];
@@ -508,12 +554,13 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     }
 }
 
-template <int D, int G, int NW, int NST, bool PART>
+template <int D, int G, int NW, int NST, int MODE>
 cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream) {
+    constexpr bool PART = MODE == MODE_PARTITION;
     constexpr size_t smem_base = decode_smem_bytes<D, G, NW, NST>();
     constexpr size_t smem_max = smem_base + size_t(kMaxSortedSeqsPartition) * 4;
     const size_t smem = smem_base + (p.order_mode == ORDER_SORTED ? size_t((p.num_seqs + 3) & ~3) * 4 : 0);
-    auto kern = paged_decode_kernel<D, G, NW, NST, PART>;
+    auto kern = paged_decode_kernel<D, G, NW, NST, MODE>;
     static std::atomic<unsigned long long> configured{0};  // one bit per device ordinal
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -531,17 +578,23 @@ cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <int D, int G, int NW, int NST>
+cudaError_t launch_decode_mode(const DecodeParams& p, int mode, cudaStream_t stream) {
+    switch (mode) {
+        case MODE_DECODE: return launch_decode_variant<D, G, NW, NST, MODE_DECODE>(p, stream);
+        case MODE_PARTITION: return launch_decode_variant<D, G, NW, NST, MODE_PARTITION>(p, stream);
+        case MODE_DECODE_APPEND: return launch_decode_variant<D, G, NW, NST, MODE_DECODE_APPEND>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <int D, int NW, int NST>
-cudaError_t launch_decode_for_dim(const DecodeParams& p, int group, bool partition, cudaStream_t stream) {
+cudaError_t launch_decode_for_dim(const DecodeParams& p, int group, int mode, cudaStream_t stream) {
     switch (group) {
-        case 1: return partition ? launch_decode_variant<D, 1, NW, NST, true>(p, stream)
-                                 : launch_decode_variant<D, 1, NW, NST, false>(p, stream);
-        case 2: return partition ? launch_decode_variant<D, 2, NW, NST, true>(p, stream)
-                                 : launch_decode_variant<D, 2, NW, NST, false>(p, stream);
-        case 4: return partition ? launch_decode_variant<D, 4, NW, NST, true>(p, stream)
-                                 : launch_decode_variant<D, 4, NW, NST, false>(p, stream);
-        case 8: return partition ? launch_decode_variant<D, 8, NW, NST, true>(p, stream)
-                                 : launch_decode_variant<D, 8, NW, NST, false>(p, stream);
+        case 1: return launch_decode_mode<D, 1, NW, NST>(p, mode, stream);
+        case 2: return launch_decode_mode<D, 2, NW, NST>(p, mode, stream);
+        case 4: return launch_decode_mode<D, 4, NW, NST>(p, mode, stream);
+        case 8: return launch_decode_mode<D, 8, NW, NST>(p, mode, stream);
         default: return cudaErrorInvalidValue;
     }
 }

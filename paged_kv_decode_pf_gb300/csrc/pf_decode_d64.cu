@@ -12,8 +12,8 @@
 
 namespace pf {
 
-cudaError_t launch_decode_d64(const DecodeParams& p, int group, bool partition, cudaStream_t stream) {
-    return launch_decode_for_dim<64, PF_D64_WARPS, PF_D64_STAGES>(p, group, partition, stream);
+cudaError_t launch_decode_d64(const DecodeParams& p, int group, int mode, cudaStream_t stream) {
+    return launch_decode_for_dim<64, PF_D64_WARPS, PF_D64_STAGES>(p, group, mode, stream);
 }
 
 }  // namespace pf

@@ -35,7 +35,18 @@ struct DecodeParams {
     int num_partitions;      // partition pass: NP
     int max_context_len;     // partition pass: bound every context length must respect
     int order_mode;          // ORDER_NATURAL or ORDER_SORTED (see below)
+    // decode with append only: the new token of sequence i, its slot, and writable caches
+    const uint16_t* k_new;   // [S, Hkv, D]
+    const uint16_t* v_new;
+    const int64_t* slot_mapping;  // [S]
+    uint16_t* k_cache_w;
+    uint16_t* v_cache_w;
 };
+
+// What one launch of the decode kernel computes.
+constexpr int MODE_DECODE = 0;          // single pass over each whole sequence
+constexpr int MODE_PARTITION = 1;       // one context partition per CTA, partials to the workspace
+constexpr int MODE_DECODE_APPEND = 2;   // single pass, after writing each sequence's new token
 
 // How CTAs map to work items.
 //  ORDER_NATURAL: CTA b serves (sequence b / Hkv, kv head b % Hkv); partition pass:
@@ -50,10 +61,15 @@ constexpr int ORDER_SORTED = 1;
 constexpr int kMaxSortedSeqsDecode = 512;      // ranking costs O(S^2 / threads) per CTA
 constexpr int kMaxSortedSeqsPartition = 1024;  // the prefix scan costs O(S / threads)
 
-// Launch the single-pass decode kernel (partition == false) or the partition
-// pass (partition == true) for one head_dim.  Returns cudaSuccess or the launch error.
-cudaError_t launch_decode_d64(const DecodeParams& p, int group, bool partition, cudaStream_t stream);
-cudaError_t launch_decode_d128(const DecodeParams& p, int group, bool partition, cudaStream_t stream);
+// Device address of the current device's error word (looked up once per device)
+// and the current device's SM count; both defined in pf_api.cu.
+cudaError_t error_word(unsigned** out);
+cudaError_t sm_count(int* out);
+
+// Launch the decode kernel in one of the MODE_* modes for one head_dim.
+// Returns cudaSuccess or the launch error.
+cudaError_t launch_decode_d64(const DecodeParams& p, int group, int mode, cudaStream_t stream);
+cudaError_t launch_decode_d128(const DecodeParams& p, int group, int mode, cudaStream_t stream);
 
 // Default bound of every device-side wait: long enough never to fire on a
 // healthy GPU (a tile copy takes microseconds), short enough to end a broken call.

@@ -39,6 +39,9 @@ MUTANTS = {
     "append_token_head_swapped": [("size_t src = ((size_t)i * num_kv_heads + h) * head_dim + c;",
                                    "size_t src = ((size_t)h * num_kv_heads + i) * head_dim + c;")],
     "append_no_skip_of_minus_one": [("if (s == -1) continue;", "")],
+    "copy_direction_swapped": [("int64_t src = block_mapping[2 * j], dst = block_mapping[2 * j + 1];",
+                                "int64_t dst = block_mapping[2 * j], src = block_mapping[2 * j + 1];")],
+    "copy_skips_v": [("            v_cache[(size_t)dst * per_block + e] = v_cache[(size_t)src * per_block + e];\n", "")],
 }
 
 

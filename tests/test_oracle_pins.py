@@ -303,3 +303,51 @@ def test_append_then_attend_sees_new_token(oracle_lib):
     appended = wl.slot_mapping >= 0
     assert np.all(np.isnan(before[appended]).any(axis=(1, 2)))
     assert np.all(np.isfinite(before[~appended]))
+
+
+# ---------------------------------------------------------------- block copy
+
+def _copy_case(seed=16):
+    wl = small(S=3, Hq=8, Hkv=2, D=64, bs=16, lengths=(20, 40, 33), seed=seed, pool_scale=3)
+    rng = np.random.default_rng(seed)
+    used = np.unique(wl.block_tables[(wl.block_tables >= 0) & (wl.block_tables < wl.num_blocks)])
+    free = np.setdiff1d(np.arange(wl.num_blocks), used)
+    src = rng.choice(used, size=4, replace=False)
+    dst = rng.choice(free, size=4, replace=False)
+    return wl, np.stack([src, dst], axis=1)
+
+
+def test_copy_blocks_matches_numpy_bit_exact(oracle_lib):
+    wl, pairs = _copy_case()
+    kc, vc, bad = oracle_lib.copy_blocks(wl.k_cache, wl.v_cache, pairs)
+    ek, ev = wl.k_cache.copy(), wl.v_cache.copy()
+    ek[pairs[:, 1]] = wl.k_cache[pairs[:, 0]]
+    ev[pairs[:, 1]] = wl.v_cache[pairs[:, 0]]
+    assert bad == 0 and np.array_equal(kc, ek) and np.array_equal(vc, ev)
+
+
+def test_copy_blocks_identity_and_out_of_range(oracle_lib):
+    wl, pairs = _copy_case(17)
+    same = np.stack([pairs[:, 0], pairs[:, 0]], axis=1)
+    kc, vc, bad = oracle_lib.copy_blocks(wl.k_cache, wl.v_cache, same)
+    assert bad == 0 and np.array_equal(kc, wl.k_cache) and np.array_equal(vc, wl.v_cache)
+    broken = np.array([[-1, pairs[0, 1]], [pairs[1, 0], wl.num_blocks], [pairs[2, 0], pairs[2, 1]]])
+    kc, vc, bad = oracle_lib.copy_blocks(wl.k_cache, wl.v_cache, broken)
+    ek = wl.k_cache.copy()
+    ek[pairs[2, 1]] = wl.k_cache[pairs[2, 0]]
+    assert bad == 2 and np.array_equal(kc, ek)
+
+
+def test_forked_sequence_attends_like_its_parent(oracle_lib):
+    """A fork copies the parent's last block into a fresh one and rewrites its table entry."""
+    wl, pairs = _copy_case(18)
+    i = 1
+    nb = int((wl.context_lens[i] + wl.block_size - 1) // wl.block_size)
+    last = wl.block_tables[i, nb - 1]
+    fresh = np.setdiff1d(np.arange(wl.num_blocks), wl.block_tables[wl.block_tables >= 0])[0]
+    kc, vc, _ = oracle_lib.copy_blocks(wl.k_cache, wl.v_cache, [[last, fresh]])
+    tables = wl.block_tables.copy()
+    tables[i, nb - 1] = fresh
+    a = oracle_lib.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    b = oracle_lib.paged_attention(wl.q, kc, vc, tables, wl.context_lens, wl.scale)
+    assert np.array_equal(a, b)
