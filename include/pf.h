@@ -216,6 +216,29 @@ PF_API pf_status pf_paged_attention_merge(const void* workspace, const int32_t* 
                                    int max_context_len, float* out, pf_stream_t stream);
 
 /*
+ * Decode attention that chooses its own decomposition from the sizes the host
+ * knows (no device memory is read): the single pass when there are enough
+ * (sequence, kv head) items to fill the GPU, otherwise the split over context
+ * partitions + merge, with a partition size that gives a long sequence enough
+ * partitions.  The result is the same attention (within fp32 rounding).
+ *
+ * pf_paged_attention_decode_auto_plan() returns the partition size the call
+ * will use (0 = single pass) and writes the workspace bytes it needs (0 for
+ * the single pass) to *workspace_bytes; it needs the current device (SM count).
+ * pf_paged_attention_decode_auto takes the decode arguments plus
+ * max_context_len (>= every context length) and a workspace of at least that
+ * size (256-byte aligned; may be NULL when the plan needs none).
+ */
+PF_API int pf_paged_attention_decode_auto_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                               int max_context_len, size_t* workspace_bytes);
+PF_API pf_status pf_paged_attention_decode_auto(const void* q, const void* k_cache, const void* v_cache,
+                                                const int32_t* block_tables, const int32_t* context_lens,
+                                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                                int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                                float scale, int max_context_len, void* workspace,
+                                                size_t workspace_bytes, float* out, pf_stream_t stream);
+
+/*
  * Device error word of the current device.  Synchronises `stream`, reads the
  * word, clears it and returns PF_ERR_DEVICE_TIMEOUT or PF_ERR_DEVICE_BOUNDS if
  * the corresponding bit was set (timeout first), PF_ERR_CUDA if the

@@ -70,6 +70,8 @@ def _bind(lib):
     lib.oracle_max_threads.restype = i32
     lib.oracle_copy_blocks.argtypes = [P, P, P, i64, i32, i32, i32, i64]
     lib.oracle_copy_blocks.restype = i64
+    lib.oracle_paged_attention_multi.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, f64, P, i32]
+    lib.oracle_paged_attention_multi.restype = None
     return lib
 
 
@@ -130,6 +132,20 @@ class Oracle:
         out = np.zeros((S, Hq, D), dtype=np.float64)
         self.lib.oracle_paged_attention(qp, kp, vp, bp, cp, S, Hq, Hkv, D, bs, bt.shape[1], float(scale),
                                         out.ctypes.data, threads)
+        return out
+
+    def paged_attention_multi(self, q, k_cache, v_cache, block_tables, context_lens, scale, threads: int = 0):
+        """q [S, q_len, Hq, D] -> out [S, q_len, Hq, D]; row (i, j) sees tokens t <= L_i - q_len + j."""
+        S, Q, Hq, D = q.shape
+        NB, Hkv, bs, _ = k_cache.shape
+        q, qp = _c(q, np.uint16)
+        kc, kp = _c(k_cache, np.uint16)
+        vc, vp = _c(v_cache, np.uint16)
+        bt, bp = _c(block_tables, np.int32)
+        cl, cp = _c(context_lens, np.int32)
+        out = np.zeros((S, Q, Hq, D), dtype=np.float64)
+        self.lib.oracle_paged_attention_multi(qp, kp, vp, bp, cp, S, Q, Hq, Hkv, D, bs, bt.shape[1], float(scale),
+                                              out.ctypes.data, threads)
         return out
 
     def paged_attention_pairs(self, q, k_cache, v_cache, block_tables, context_lens, scale, pairs,

@@ -33,6 +33,11 @@
  *        out = sum_k w_k o_k / sum_k w_k.
  *    Empty partitions are written as m = -inf, l = 0, o = 0.
  *
+ *  - Several query tokens per sequence: the same attention for query row
+ *    (i, j, h) over the tokens t <= L_i - q_len + j (see
+ *    oracle_paged_attention_multi).  Block copy: whole physical blocks, bit
+ *    for bit (oracle_copy_blocks).
+ *
  * bf16 inputs are decoded here, independently of any CUDA header: a bf16 bit
  * pattern is the top half of an IEEE binary32, so widening is exact.
  */
@@ -118,11 +123,19 @@ typedef struct {
     double scale;
 } problem_t;
 
-/* Scores s_t for tokens [t0, t1) of (seq i, q head h) into s[0 .. t1-t0). */
-static void scores(const problem_t* P, int i, int h, int t0, int t1, double* s) {
+/* Grouped-query map: query head h reads kv head h / g, g = Hq / Hkv. */
+static int kv_head_of(const problem_t* P, int h) {
     int g = P->Hq / P->Hkv;
-    int kh = h / g;
-    const uint16_t* qv = P->q + ((size_t)i * P->Hq + h) * P->D;
+    return h / g;
+}
+
+/* The query vector of (sequence i, head h) in a [S][Hq][D] query. */
+static const uint16_t* query_row(const problem_t* P, int i, int h) {
+    return P->q + ((size_t)i * P->Hq + h) * P->D;
+}
+
+/* Scores s_t = scale * qv . K_t for tokens [t0, t1) of sequence i, kv head kh. */
+static void scores(const problem_t* P, const uint16_t* qv, int i, int kh, int t0, int t1, double* s) {
     for (int t = t0; t < t1; ++t) {
         int64_t p = P->block_tables[(size_t)i * P->MB + t / P->bs];
         int off = t % P->bs;
@@ -135,13 +148,11 @@ static void scores(const problem_t* P, int i, int h, int t0, int t1, double* s) 
 
 /* Softmax-weighted sum of V over tokens [t0, t1): o = sum_t e_t V_t / sum_t e_t with
  * e_t = exp(s_t - m), m = max s_t.  Also returns m and l = sum e_t. */
-static void attend_range(const problem_t* P, int i, int h, int t0, int t1, double* s, double* o,
-                         double* m_out, double* l_out) {
-    int g = P->Hq / P->Hkv;
-    int kh = h / g;
+static void attend_range(const problem_t* P, const uint16_t* qv, int i, int kh, int t0, int t1, double* s,
+                         double* o, double* m_out, double* l_out) {
     for (int c = 0; c < P->D; ++c) o[c] = 0.0;
     if (t1 <= t0) { *m_out = -INFINITY; *l_out = 0.0; return; }
-    scores(P, i, h, t0, t1, s);
+    scores(P, qv, i, kh, t0, t1, s);
     double m = -INFINITY;
     for (int t = 0; t < t1 - t0; ++t) if (s[t] > m) m = s[t];
     double l = 0.0;
@@ -184,7 +195,7 @@ void oracle_paged_attention(const uint16_t* q, const uint16_t* k_cache, const ui
         int L = context_lens[i];
         double* s = (double*)malloc(sizeof(double) * (L > 0 ? L : 1));
         double m, l;
-        attend_range(&P, i, h, 0, L, s, out + (size_t)ph * head_dim, &m, &l);
+        attend_range(&P, query_row(&P, i, h), i, kv_head_of(&P, h), 0, L, s, out + (size_t)ph * head_dim, &m, &l);
         free(s);
     }
 }
@@ -206,7 +217,42 @@ void oracle_paged_attention_pairs(const uint16_t* q, const uint16_t* k_cache, co
         int L = context_lens[i];
         double* s = (double*)malloc(sizeof(double) * (L > 0 ? L : 1));
         double m, l;
-        attend_range(&P, i, h, 0, L, s, out + (size_t)j * head_dim, &m, &l);
+        attend_range(&P, query_row(&P, i, h), i, kv_head_of(&P, h), 0, L, s, out + (size_t)j * head_dim, &m, &l);
+        free(s);
+    }
+}
+
+/* ------------------------------------------------- multi-token query rows */
+
+/* Several new tokens per sequence (a chunk of a long prompt interleaved with
+ * decode -- "long prompts are split into bounded chunks and interleaved with
+ * decode", ForgeLLM README -- or the draft tokens a speculative step verifies,
+ * TokenForge post): sequence i has q_len new tokens at positions
+ * L_i - q_len + j, j < q_len, already in the cache; query row (i, j, h) attends
+ * to the tokens t <= L_i - q_len + j (causal among the new tokens).  A row whose
+ * position is negative (L_i < q_len) is zero.
+ * q, out: [S][q_len][Hq][D]. */
+void oracle_paged_attention_multi(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                  const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                  int q_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, double scale, double* out, int num_threads) {
+    problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_q_heads, num_kv_heads,
+                   head_dim, block_size, max_blocks_per_seq, scale};
+    set_threads(num_threads);
+    int64_t rows = (int64_t)num_seqs * q_len * num_q_heads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t r = 0; r < rows; ++r) {
+        int i = (int)(r / ((int64_t)q_len * num_q_heads));
+        int j = (int)((r / num_q_heads) % q_len);
+        int h = (int)(r % num_q_heads);
+        int pos = context_lens[i] - q_len + j;
+        int t1 = pos + 1;
+        const uint16_t* qv = q + (size_t)r * head_dim;
+        double* s = (double*)malloc(sizeof(double) * (t1 > 0 ? t1 : 1));
+        double m, l;
+        attend_range(&P, qv, i, kv_head_of(&P, h), 0, t1 > 0 ? t1 : 0, s, out + (size_t)r * head_dim, &m, &l);
         free(s);
     }
 }
@@ -235,7 +281,8 @@ void oracle_paged_attention_partition(const uint16_t* q, const uint16_t* k_cache
             int t0 = k * partition_size;
             int t1 = t0 + partition_size < L ? t0 + partition_size : L;
             size_t slot = (size_t)ph * max_partitions + k;
-            attend_range(&P, i, h, t0, t1, s, tmp_out + slot * head_dim, &tmp_m[slot], &tmp_l[slot]);
+            attend_range(&P, query_row(&P, i, h), i, kv_head_of(&P, h), t0, t1, s, tmp_out + slot * head_dim,
+                         &tmp_m[slot], &tmp_l[slot]);
         }
         free(s);
     }

@@ -78,6 +78,11 @@ def lib() -> ctypes.CDLL:
         L.pf_paged_attention_decode_append.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
                                                        f32, P, P]
         L.pf_paged_attention_decode_append.restype = st
+        L.pf_paged_attention_decode_auto_plan.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
+        L.pf_paged_attention_decode_auto_plan.restype = i32
+        L.pf_paged_attention_decode_auto.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, f32, i32, P,
+                                                     sz, P, P]
+        L.pf_paged_attention_decode_auto.restype = st
         _LIB = L
     return _LIB
 
@@ -194,6 +199,41 @@ def paged_attention_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: t
             q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), k_cache.data_ptr(),
             v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), S, Hq, Hkv, D, bs, MB, NB, scale,
             out.data_ptr(), _stream(q.device)), "pf_paged_attention_decode_append")
+    return out
+
+
+def decode_auto_plan(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                     max_context_len: int, device=None) -> Tuple[int, int]:
+    """(partition size the auto decode will use, 0 = single pass; workspace bytes it needs)."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    ws = ctypes.c_size_t()
+    with torch.cuda.device(device):
+        P = lib().pf_paged_attention_decode_auto_plan(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                      max_context_len, ctypes.byref(ws))
+    return int(P), ws.value
+
+
+def paged_attention_decode_auto(q, k_cache, v_cache, block_tables, context_lens, max_context_len: Optional[int] = None,
+                                scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
+                                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode attention with the decomposition chosen by the library (single pass or split + merge).
+    max_context_len defaults to the table's capacity; a workspace is allocated when the plan needs one."""
+    S, Hq, Hkv, D, bs, NB, MB = _attn_shapes(q, k_cache, v_cache, block_tables, context_lens)
+    if max_context_len is None:
+        max_context_len = MB * bs
+    P, need = decode_auto_plan(S, Hq, Hkv, D, max_context_len, q.device)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((S, Hq, D), dtype=torch.float32, device=q.device)
+    _cuda(out, "out", (torch.float32,), 3)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    with torch.cuda.device(q.device):
+        _check(lib().pf_paged_attention_decode_auto(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
+            S, Hq, Hkv, D, bs, MB, NB, scale, max_context_len, ws_ptr, ws_bytes, out.data_ptr(),
+            _stream(q.device)), "pf_paged_attention_decode_auto")
     return out
 
 

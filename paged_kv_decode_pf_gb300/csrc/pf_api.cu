@@ -495,3 +495,60 @@ pf_status pf_debug_bounded_wait(int64_t limit_ns, pf_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ======================================================== auto decomposition
+
+namespace pf {
+// Decode CTAs resident per SM at the compiled configuration (shared memory bound).
+constexpr int kDecodeCtasPerSm = 3;
+}  // namespace pf
+
+extern "C" {
+
+int pf_paged_attention_decode_auto_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                        int max_context_len, size_t* workspace_bytes) {
+    if (workspace_bytes) *workspace_bytes = 0;
+    if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess || sms <= 0) return 0;
+    const long long slots = (long long)sms * kDecodeCtasPerSm;
+    const long long items = (long long)num_seqs * num_kv_heads;
+    // Enough (sequence, kv head) items, or short contexts: one pass, ordered longest first.
+    if (items >= 2 * slots || max_context_len <= 1024) return 0;
+    // Otherwise split so that one sequence of the longest length alone spreads over about
+    // two CTAs per slot: P = the largest power of two <= max_len * Hkv / (2 * slots), >= 256.
+    const long long target = (long long)max_context_len * num_kv_heads / (2 * slots);
+    int P = 256;
+    while ((long long)P * 2 <= target && P < (1 << 16)) P *= 2;
+    const size_t need =
+        pf_paged_attention_partition_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len, P);
+    if (need == 0) return 0;
+    if (workspace_bytes) *workspace_bytes = need;
+    return P;
+}
+
+pf_status pf_paged_attention_decode_auto(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                         int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                         int max_context_len, void* workspace, size_t workspace_bytes, float* out,
+                                         pf_stream_t stream) {
+    if (max_context_len < 0) return PF_ERR_INVALID_ARG;
+    size_t need = 0;
+    const int P = pf_paged_attention_decode_auto_plan(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                      max_context_len, &need);
+    if (P == 0)
+        return pf_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                                         num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                                         out, stream);
+    if (workspace_bytes < need || !aligned(workspace, 256)) return PF_ERR_INVALID_ARG;
+    pf_status st = pf_paged_attention_decode_partition(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                                       num_q_heads, num_kv_heads, head_dim, block_size,
+                                                       max_blocks_per_seq, num_blocks, scale, P, max_context_len,
+                                                       workspace, workspace_bytes, stream);
+    if (st != PF_OK) return st;
+    return pf_paged_attention_merge(workspace, context_lens, num_seqs, num_q_heads, head_dim, P, max_context_len,
+                                    out, stream);
+}
+
+}  // extern "C"

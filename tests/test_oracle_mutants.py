@@ -17,7 +17,7 @@ import oracle
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 MUTANTS = {
-    "gqa_interleaved_head_map": [("int kh = h / g;", "int kh = h % P->Hkv;")],
+    "gqa_interleaved_head_map": [("    return h / g;", "    return h % P->Hkv;")],
     "dropped_scale": [("s[t - t0] = P->scale * dot;", "s[t - t0] = dot;")],
     "score_sign": [("dot += bf16_to_f64(qv[c])", "dot -= bf16_to_f64(qv[c])")],
     "reversed_offset_in_block": [("int off = t % P->bs;", "int off = (P->bs - 1) - t % P->bs;")],
@@ -41,6 +41,8 @@ MUTANTS = {
     "append_no_skip_of_minus_one": [("if (s == -1) continue;", "")],
     "copy_direction_swapped": [("int64_t src = block_mapping[2 * j], dst = block_mapping[2 * j + 1];",
                                 "int64_t dst = block_mapping[2 * j], src = block_mapping[2 * j + 1];")],
+    "multi_query_not_causal": [("int t1 = pos + 1;", "int t1 = context_lens[i];")],
+    "multi_query_row_off_by_one": [("int pos = context_lens[i] - q_len + j;", "int pos = context_lens[i] - q_len + j - 1;")],
     "copy_skips_v": [("            v_cache[(size_t)dst * per_block + e] = v_cache[(size_t)src * per_block + e];\n", "")],
 }
 

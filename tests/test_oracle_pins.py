@@ -351,3 +351,53 @@ def test_forked_sequence_attends_like_its_parent(oracle_lib):
     a = oracle_lib.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
     b = oracle_lib.paged_attention(wl.q, kc, vc, tables, wl.context_lens, wl.scale)
     assert np.array_equal(a, b)
+
+
+# --------------------------------------------------------- multi-token query
+
+def _multi(wl, Q):
+    from workloads import multi_query
+    return multi_query(wl, Q)
+
+
+def test_multi_query_single_token_is_decode(oracle_lib):
+    wl = small(S=3, Hq=8, Hkv=2, lengths=(5, 40, 64), seed=19)
+    q = wl.q[:, None]                                        # [S, 1, Hq, D]
+    m = oracle_lib.paged_attention_multi(q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    assert np.array_equal(m[:, 0], run(oracle_lib, wl))
+
+
+def test_multi_query_rows_are_decodes_of_their_prefix(oracle_lib):
+    """Row j of sequence i equals a decode of query q[i, j] over the first L_i - Q + j + 1 tokens."""
+    wl = small(S=3, Hq=4, Hkv=2, lengths=(9, 33, 60), seed=20)
+    Q = 5
+    q = _multi(wl, Q)
+    m = oracle_lib.paged_attention_multi(q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    for j in range(Q):
+        lens = (wl.context_lens - Q + j + 1).astype(np.int32)
+        ref = oracle_lib.paged_attention(q[:, j], wl.k_cache, wl.v_cache, wl.block_tables, lens, wl.scale)
+        assert np.array_equal(m[:, j], ref)
+
+
+def test_multi_query_dense_bruteforce_causal(oracle_lib):
+    wl = small(S=2, Hq=4, Hkv=1, D=64, lengths=(7, 20), seed=21)
+    Q = 4
+    q = _multi(wl, Q)
+    m = oracle_lib.paged_attention_multi(q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    qf = bf16_bits_to_f32(q).astype(np.float64)
+    for i in range(wl.num_seqs):
+        K, V = gather_kv(wl, i)
+        L = int(wl.context_lens[i])
+        for j in range(Q):
+            pos = L - Q + j
+            for h in range(wl.num_q_heads):
+                ref = dense.attention(list(qf[i, j, h]), K[:pos + 1, 0].tolist(), V[:pos + 1, 0].tolist(), wl.scale)
+                np.testing.assert_allclose(m[i, j, h], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_multi_query_rows_before_the_sequence_start_are_zero(oracle_lib):
+    wl = small(S=2, Hq=2, Hkv=1, lengths=(2, 30), seed=22)
+    Q = 4                                                     # sequence 0 has only 2 tokens
+    m = oracle_lib.paged_attention_multi(_multi(wl, Q), wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
+                                         wl.scale)
+    assert not m[0, :2].any() and np.all(np.isfinite(m[0, 2:])) and m[0, 2:].any()

@@ -267,6 +267,15 @@ def make_workload(name: str, num_seqs: int, num_q_heads: int, num_kv_heads: int,
     return wl
 
 
+STREAM_MULTI_Q = 6
+
+
+def multi_query(wl: Workload, q_len: int, threads: int = 0) -> np.ndarray:
+    """Queries of q_len new tokens per sequence, [S, q_len, Hq, D] bf16 bits (the tokens
+    themselves are the last q_len positions already in the workload's cache)."""
+    return normal_bf16((wl.num_seqs, q_len, wl.num_q_heads, wl.head_dim), wl.seed, STREAM_MULTI_Q, threads=threads)
+
+
 def _times_pow2(bits: np.ndarray, factor: int) -> np.ndarray:
     x = bf16_bits_to_f32(bits) * np.float32(factor)
     return f32_to_bf16_bits(x)
