@@ -303,6 +303,34 @@ def job_throughput(world, bytes_per_step_per_rank, ms_per_step):
     return world * bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
+class MultiQueryRunner:
+    """pf_paged_attention_multi_query over a resident workload: the last q_len tokens of
+    every sequence are its new tokens (draft tokens under verification)."""
+
+    def __init__(self, pf, runner, q_len):
+        import torch
+        from workloads import multi_query
+        self.pf, self.r, self.q_len = pf, runner, q_len
+        wl = runner.wl
+        q = multi_query(wl, q_len)
+        self.q = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).view(torch.bfloat16).to(runner.dev)
+        self.out = torch.empty((wl.num_seqs, q_len, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
+                               device=runner.dev)
+
+    def step(self, ev=None):
+        r = self.r
+        if ev is not None:
+            ev[0].record()
+        self.pf.paged_attention_multi_query(self.q, r.kc, r.vc, r.bt, r.cl, r.wl.scale, self.out)
+        if ev is not None:
+            ev[1].record()
+
+    def step_bytes(self):
+        wl = self.r.wl
+        rows = wl.num_seqs * self.q_len * wl.num_q_heads * wl.head_dim
+        return wl.algorithmic_bytes() - wl.num_seqs * wl.num_q_heads * wl.head_dim * 6 + rows * 6
+
+
 class CopyRunner:
     """pf_copy_blocks over `pairs` random (src, dst) pairs of Llama-3-8B-shaped blocks
     (8 kv heads x 16 tokens x 128 dims, bf16): a pure read + write stream."""
@@ -445,6 +473,21 @@ def main():
 
     extras = {}
     if not args.no_extras and rank == 0:
+        if not runner.split and wl.num_q_heads // wl.num_kv_heads * 4 <= 16:
+            # the same resident cache, with the last 4 tokens of every sequence as new (draft) tokens
+            mr = MultiQueryRunner(pf, runner, 4)
+            ms_s, ms_d, _ = time_steps(mr, 200, 10)
+            pf.check_device_error()
+            mb = mr.step_bytes()
+            extras[CONFIGS[args.workload].name + "_multi_query_q4"] = {
+                "description": "pf_paged_attention_multi_query on the same cache: 4 new tokens per sequence, "
+                               "causal among them",
+                "step": "multi_query", "us_dominant_kernel": round(ms_d * 1e3, 2), "algorithmic_bytes": mb,
+                "gbs_dominant_kernel": round(mb / (ms_d * 1e-3) / 1e9, 1),
+                "pct_of_8tbs_dominant": round(100 * mb / (ms_d * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
+                "l2": "inputs larger than L2",
+            }
+            del mr
         del runner
         torch.cuda.empty_cache()
         for idx, variant in [(1, "decode"), (2, "decode"), (3, "decode"), (3, "fused"), (5, "decode")]:

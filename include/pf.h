@@ -166,6 +166,33 @@ PF_API pf_status pf_paged_attention_decode_append(const void* q, const void* k_n
                                                   float scale, float* out, pf_stream_t stream);
 
 /*
+ * Several new tokens per sequence at once: the draft tokens a speculative step
+ * verifies ("paired the main model with a tiny draft model to guess tokens
+ * ahead of time", TokenForge post) or a short prompt chunk interleaved with
+ * decode ("long prompts are split into bounded chunks and interleaved with
+ * decode", ForgeLLM README).  The q_len new tokens of sequence i are its last
+ * positions L_i - q_len + j, already in the cache; query row (j, h) attends to
+ * the tokens t <= L_i - q_len + j:
+ *
+ *   out[i][j][h][:] = sum_{t <= L_i - q_len + j} softmax_t(scale * q[i][j][h] . K_t) V_t
+ *
+ * A row whose position is negative (L_i < q_len) is zero.  The scores and P.V
+ * run on tensor cores (mma.sync, bf16 inputs, fp32 accumulation; the
+ * probabilities enter P.V as a bf16 high part plus a bf16 remainder).
+ *
+ *   q    [num_seqs, q_len, num_q_heads, head_dim] bf16, 16-byte aligned
+ *   out  [num_seqs, q_len, num_q_heads, head_dim] fp32
+ * Supported: head_dim in {64, 128}, block_size a multiple of 16,
+ * (num_q_heads / num_kv_heads) * q_len <= 16, num_blocks * num_kv_heads *
+ * block_size < 2^31; other arguments and errors as pf_paged_attention_decode.
+ */
+PF_API pf_status pf_paged_attention_multi_query(const void* q, const void* k_cache, const void* v_cache,
+                                                const int32_t* block_tables, const int32_t* context_lens,
+                                                int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                                int head_dim, int block_size, int max_blocks_per_seq,
+                                                int64_t num_blocks, float scale, float* out, pf_stream_t stream);
+
+/*
  * Split over context partitions ("flash-decoding") for long contexts.
  *
  * The workspace holds, for NP = ceil(max_context_len / partition_size)

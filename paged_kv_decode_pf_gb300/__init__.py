@@ -83,6 +83,9 @@ def lib() -> ctypes.CDLL:
         L.pf_paged_attention_decode_auto.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, f32, i32, P,
                                                      sz, P, P]
         L.pf_paged_attention_decode_auto.restype = st
+        L.pf_paged_attention_multi_query.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i64, f32, P,
+                                                     P]
+        L.pf_paged_attention_multi_query.restype = st
         _LIB = L
     return _LIB
 
@@ -199,6 +202,33 @@ def paged_attention_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: t
             q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), k_cache.data_ptr(),
             v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), S, Hq, Hkv, D, bs, MB, NB, scale,
             out.data_ptr(), _stream(q.device)), "pf_paged_attention_decode_append")
+    return out
+
+
+def paged_attention_multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                scale: Optional[float] = None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """q [S, q_len, Hq, D]: the last q_len tokens of each sequence, already in the cache, attend causally.
+    Returns out [S, q_len, Hq, D] fp32.  Needs (Hq / Hkv) * q_len <= 16."""
+    _cuda(q, "q", _BF16, 4)
+    _cuda(k_cache, "k_cache", _BF16, 4)
+    _cuda(v_cache, "v_cache", _BF16, 4)
+    _cuda(block_tables, "block_tables", (torch.int32,), 2)
+    _cuda(context_lens, "context_lens", (torch.int32,), 1)
+    S, Q, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D or block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("paged_attention_multi_query: inconsistent shapes")
+    MB = block_tables.shape[1]
+    if out is None:
+        out = torch.empty((S, Q, Hq, D), dtype=torch.float32, device=q.device)
+    _cuda(out, "out", (torch.float32,), 4)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        _check(lib().pf_paged_attention_multi_query(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                                    block_tables.data_ptr(), context_lens.data_ptr(), S, Q, Hq, Hkv,
+                                                    D, bs, MB, NB, scale, out.data_ptr(), _stream(q.device)),
+               "pf_paged_attention_multi_query")
     return out
 
 

@@ -1,0 +1,449 @@
+// Multi-token paged query: pf_paged_attention_multi_query.
+//
+// Several new tokens per sequence attend over the paged cache at once -- the
+// draft tokens a speculative step verifies (TokenForge post: "paired the main
+// model with a tiny draft model to guess tokens ahead of time") or a short chunk
+// of a prompt interleaved with decode (ForgeLLM README: "long prompts are split
+// into bounded chunks and interleaved with decode").  Sequence i has q_len new
+// tokens at positions L_i - q_len + j, already in the cache; query row (j, h)
+// sees the tokens t <= L_i - q_len + j.
+//
+// With R = g * q_len query rows per kv head the scores are a real (small)
+// contraction, [R x D] . [D x 16] per tile, so this kernel runs both products on
+// the tensor cores:
+//  * One CTA per (sequence, kv head); 4 warps split the 16-token tiles as in the
+//    decode kernel, each with its own 2-stage ring; lane 0 issues TMA tensor
+//    copies (cp.async.bulk.tensor) of the K and V tiles with the 128-byte swizzle,
+//    so the ldmatrix reads below are free of bank conflicts.
+//  * S = Q K^T with mma.sync m16n8k16 (bf16 in, fp32 accumulate): Q (R <= 16 rows,
+//    zero-padded) lives in registers as A fragments, K^T comes from ldmatrix.
+//  * Per-row causal limits, an fp32 online softmax on the accumulator fragments
+//    (quad shuffles), then P.V: P is split into bf16 hi + lo parts (two MMAs
+//    against the same V fragments, ldmatrix.trans) so the probabilities keep
+//    about 16 significant bits.
+//  * The 4 warps merge (m, l, O) in shared memory at the end.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include <cuda.h>  // CUtensorMap and its enums only; the encoder is fetched from the runtime
+#include <cuda_runtime.h>
+
+#include "pf.h"
+#include "pf_device.cuh"
+#include "pf_internal.h"
+
+namespace pf {
+
+constexpr int kMultiMaxRows = 16;  // g * q_len: one m16 tile of query rows
+
+struct MultiParams {
+    const uint16_t* q;          // [S, q_len, Hq, D]
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float* out;                 // [S, q_len, Hq, D]
+    unsigned* err;
+    long long num_blocks;
+    unsigned long long wait_limit_ns;
+    float scale_log2;
+    int num_seqs, q_len, num_q_heads, num_kv_heads, group, rows;
+    int block_size, block_shift, max_blocks_per_seq;
+};
+
+template <int D, int NW, int NST>
+struct MultiLayout {
+    static constexpr int TT = kTileTokens;
+    static constexpr int HALVES = D / 64;                // 128-byte swizzle rows per token row
+    static constexpr int HALF_BYTES = TT * 128;          // one TMA box: 16 rows x 128 B
+    static constexpr int TILE = HALVES * HALF_BYTES;     // K or V tile, 16 x D bf16
+    static constexpr int STAGE = 2 * TILE;
+    static constexpr size_t STAGES_BYTES = size_t(NW) * NST * STAGE;
+    static constexpr size_t BARS = STAGES_BYTES;                          // NW*NST mbarriers
+    static constexpr size_t FLAGS = BARS + size_t(NW) * NST * 8;           // NW ints
+    static constexpr size_t ML = FLAGS + ((NW * 4 + 15) / 16) * 16;        // [NW][2][16] floats
+    static constexpr size_t BYTES = ML + size_t(NW) * 2 * kMultiMaxRows * 4;
+    static constexpr size_t ALLOC = BYTES + 1024;                          // room to align to 1024
+    static_assert(NST * STAGE >= kMultiMaxRows * D * 4, "stage area holds a warp's O for the merge");
+};
+
+template <int D, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32) paged_multi_query_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                                                     const __grid_constant__ CUtensorMap tmap_v,
+                                                                     const MultiParams p) {
+    using Lay = MultiLayout<D, NW, NST>;
+    constexpr int TT = Lay::TT, HALVES = Lay::HALVES, HALF = Lay::HALF_BYTES, TILE = Lay::TILE;
+    constexpr int STAGE = Lay::STAGE;
+    constexpr int KSTEPS = D / 16;  // k-steps of S = Q K^T
+    constexpr int NTD = D / 8;      // n-tiles of O = P V
+    constexpr int R = NST + 2;      // table entries lane 0 holds ahead of the copies
+
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // swizzled boxes need 1 KiB alignment
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::BARS);
+    int* flags = reinterpret_cast<int*>(smem + Lay::FLAGS);
+    float* ml = reinterpret_cast<float*>(smem + Lay::ML);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int Hkv = p.num_kv_heads, G = p.group, Q = p.q_len, RR = p.rows, Hq = p.num_q_heads;
+    const int seq = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
+    const int L = __ldg(p.context_lens + seq);
+    const bool len_bad = L < 0 || (long long)L > (long long)p.max_blocks_per_seq * p.block_size;
+    auto out_row = [&](int r) -> float* {  // query row r = j * G + h
+        const int j = r / G, h = r - (r / G) * G;
+        return p.out + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D;
+    };
+    if (len_bad) {
+        if (threadIdx.x == 0) set_error(p.err, ERR_BOUNDS);
+        for (int e = threadIdx.x; e < RR * D; e += NW * 32) out_row(e / D)[e % D] = NAN;
+        return;
+    }
+
+    const int ntiles = (L + TT - 1) / TT;
+    const int nk = ntiles > warp ? (ntiles - warp + NW - 1) / NW : 0;
+    unsigned char* my_stages = smem + size_t(warp) * NST * STAGE;
+    const uint32_t stage0 = smem_u32(my_stages);
+    const uint32_t bar0 = smem_u32(bars + warp * NST);
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < NST; ++s) mbar_init(bar0 + 8 * s, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+
+    // ---- producer (lane 0): TMA boxes of the warp's tiles, table entries NST+2 ahead
+    const int32_t* trow = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
+    const int bs = p.block_size, bshift = p.block_shift;
+    auto block_index = [&](int tok) { return bshift >= 0 ? (tok >> bshift) : (tok / bs); };
+    auto block_offset = [&](int tok) { return bshift >= 0 ? (tok & (bs - 1)) : (tok % bs); };
+    auto tile_token = [&](int k) { return (warp + k * NW) * TT; };
+    int ent[R];
+    bool bad_block = false;
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](int k, int pb) {
+        const int s = k % NST;
+        const uint32_t bar = bar0 + 8 * s;
+        if (pb >= 0 && (long long)pb < p.num_blocks) {
+            const int tok = tile_token(k);
+            const int y = (pb * Hkv + kvh) * bs + block_offset(tok);
+            const uint32_t dst = stage0 + uint32_t(s) * STAGE;
+            mbar_arrive_expect_tx(bar, STAGE);
+#pragma unroll
+            for (int hh = 0; hh < HALVES; ++hh) {
+                tma_load_2d(dst + hh * HALF, &tmap_k, hh * 64, y, bar, policy);
+                tma_load_2d(dst + TILE + hh * HALF, &tmap_v, hh * 64, y, bar, policy);
+            }
+        } else {
+            bad_block = true;
+            mbar_arrive(bar);
+        }
+    };
+    auto advance = [&](int k_next_load) {
+#pragma unroll
+        for (int j = 0; j < R - 1; ++j) ent[j] = ent[j + 1];
+        ent[R - 1] = k_next_load < nk ? __ldg(trow + block_index(tile_token(k_next_load))) : 0;
+    };
+    if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) ent[j] = j < nk ? __ldg(trow + block_index(tile_token(j))) : 0;
+#pragma unroll
+        for (int k = 0; k < NST; ++k)
+            if (k < nk) {
+                issue(k, ent[0]);
+                advance(k + R);
+            }
+    }
+
+    // ---- query rows g and g+8 of the m16 tile as A fragments (zero rows past RR)
+    const int r0 = g, r1 = g + 8;
+    auto qrow = [&](int r) -> const uint16_t* {
+        const int j = r / G, h = r - (r / G) * G;
+        return p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D;
+    };
+    uint32_t qa[KSTEPS][4];
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+        const int c = ks * 16 + 2 * t;
+        qa[ks][0] = r0 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r0) + c)) : 0u;
+        qa[ks][1] = r1 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r1) + c)) : 0u;
+        qa[ks][2] = r0 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r0) + c + 8)) : 0u;
+        qa[ks][3] = r1 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r1) + c + 8)) : 0u;
+    }
+    // tokens t < lim are visible to a row; padding rows see nothing
+    const int lim0 = r0 < RR ? L - Q + r0 / G + 1 : 0;
+    const int lim1 = r1 < RR ? L - Q + r1 / G + 1 : 0;
+
+    float o[NTD][4];
+#pragma unroll
+    for (int n = 0; n < NTD; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    // swizzled byte offset of 16-byte chunk c (0 .. D/8-1) of token row `tok` in a tile
+    auto swz = [](int tok, int c) { return (c >> 3) * HALF + tok * 128 + (((c & 7) ^ (tok & 7)) << 4); };
+
+    bool timed_out = false;
+    int k = 0;
+    for (; k < nk; ++k) {
+        const int s = k % NST;
+        const bool ok = mbar_wait_bounded(bar0 + 8 * s, (k / NST) & 1, p.wait_limit_ns);
+        if (__any_sync(FULL_MASK, !ok)) { timed_out = true; break; }
+        unsigned char* Ks = my_stages + size_t(s) * STAGE;
+        unsigned char* Vs = Ks + TILE;
+        const uint32_t ks_addr = smem_u32(Ks), vs_addr = smem_u32(Vs);
+        const int tok0 = tile_token(k);
+        const int nvalid = min(TT, L - tok0);
+        if (nvalid < TT) {
+            // rows past the sequence hold other data (or poison): zero V there so 0 * V stays 0
+            for (int b = lane; b < (TT - nvalid) * HALVES * 8; b += 32) {
+                const int row = nvalid + b / (HALVES * 8), rest = b % (HALVES * 8);
+                *reinterpret_cast<uint4*>(Vs + (rest >> 3) * HALF + row * 128 + (rest & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+        }
+
+        // -- S = Q K^T for the 16 tokens: two n-tiles of 8
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kp = 0; kp < KSTEPS / 2; ++kp) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int tok = nt * 8 + (lane & 7);
+                const int c = kp * 4 + (lane >> 3);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(ks_addr + swz(tok, c), b0, b1, b2, b3);
+                mma_bf16_16816(sc[nt], qa[2 * kp], b0, b1);
+                mma_bf16_16816(sc[nt], qa[2 * kp + 1], b2, b3);
+            }
+        }
+        // -- mask, scale to base 2, online softmax per row (the 4 lanes of a quad share a row)
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tok = tok0 + nt * 8 + 2 * t + (e & 1);
+                const bool vis = tok < (e < 2 ? lim0 : lim1);
+                sc[nt][e] = vis ? sc[nt][e] * p.scale_log2 : -INFINITY;
+                if (e < 2) mx0 = fmaxf(mx0, sc[nt][e]); else mx1 = fmaxf(mx1, sc[nt][e]);
+            }
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float sf0 = mn0 == -INFINITY ? 0.f : mn0, sf1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = exp2_approx(m0 - sf0), al1 = exp2_approx(m1 - sf1);
+        m0 = mn0;
+        m1 = mn1;
+        float pr[2][4];
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                pr[nt][e] = exp2_approx(sc[nt][e] - (e < 2 ? sf0 : sf1));
+                if (e < 2) ps0 += pr[nt][e]; else ps1 += pr[nt][e];
+            }
+        l0 = l0 * al0 + ps0;
+        l1 = l1 * al1 + ps1;
+#pragma unroll
+        for (int n = 0; n < NTD; ++n) {
+            o[n][0] *= al0; o[n][1] *= al0;
+            o[n][2] *= al1; o[n][3] *= al1;
+        }
+        // -- P as A fragments, split into bf16 hi + lo
+        uint32_t ph[4], pl[4];
+        {
+            const float* v[4] = {&pr[0][0], &pr[0][2], &pr[1][0], &pr[1][2]};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float a = v[i][0], b = v[i][1];
+                ph[i] = pack_bf16x2(a, b);
+                const float ah = __uint_as_float(ph[i] << 16), bh = __uint_as_float(ph[i] & 0xffff0000u);
+                pl[i] = pack_bf16x2(a - ah, b - bh);
+            }
+        }
+        // -- O += P V: V fragments via ldmatrix.trans, two n-tiles of 8 dims per load
+#pragma unroll
+        for (int dp = 0; dp < NTD / 2; ++dp) {
+            const int mi = lane >> 3;
+            const int tok = ((mi & 1) << 3) + (lane & 7);
+            const int c = 2 * dp + (mi >> 1);
+            uint32_t v0, v1, v2, v3;
+            ldmatrix_x4_trans(vs_addr + swz(tok, c), v0, v1, v2, v3);
+            mma_bf16_16816(o[2 * dp], ph, v0, v1);
+            mma_bf16_16816(o[2 * dp], pl, v0, v1);
+            mma_bf16_16816(o[2 * dp + 1], ph, v2, v3);
+            mma_bf16_16816(o[2 * dp + 1], pl, v2, v3);
+        }
+        __syncwarp();
+        if (lane == 0 && k + NST < nk) {
+            issue(k + NST, ent[0]);
+            advance(k + NST + R);
+        }
+    }
+
+    if (timed_out) {
+        if (lane == 0) set_error(p.err, ERR_TIMEOUT);
+        const int last = min(k + NST, nk);
+        for (int kk = k; kk < last; ++kk) mbar_wait_bounded(bar0 + 8 * (kk % NST), (kk / NST) & 1, p.wait_limit_ns);
+    }
+    if (lane == 0 && bad_block) set_error(p.err, ERR_BOUNDS);
+    const bool warp_failed = __any_sync(FULL_MASK, bad_block || timed_out);
+
+    // ---- row sums over the quad, then stash (m, l, O) of this warp
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+        l0 += __shfl_xor_sync(FULL_MASK, l0, off);
+        l1 += __shfl_xor_sync(FULL_MASK, l1, off);
+    }
+    __syncwarp();
+    float* mlw = ml + warp * 2 * kMultiMaxRows;
+    if (t == 0) {
+        mlw[r0] = m0; mlw[r1] = m1;
+        mlw[kMultiMaxRows + r0] = l0; mlw[kMultiMaxRows + r1] = l1;
+    }
+    float* ow = reinterpret_cast<float*>(my_stages);  // [16 rows][D]
+#pragma unroll
+    for (int n = 0; n < NTD; ++n) {
+        *reinterpret_cast<float2*>(ow + r0 * D + n * 8 + 2 * t) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(ow + r1 * D + n * 8 + 2 * t) = make_float2(o[n][2], o[n][3]);
+    }
+    if (lane == 0) flags[warp] = warp_failed ? 1 : 0;
+    __syncthreads();
+
+    // ---- merge the warps and write the RR real rows
+    bool failed = false;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) failed = failed || flags[w] != 0;
+    for (int e = threadIdx.x; e < RR * D; e += NW * 32) {
+        const int r = e / D, d = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, ml[w * 2 * kMultiMaxRows + r]);
+        float wsum = 0.f, acc = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float f = exp2_approx(ml[w * 2 * kMultiMaxRows + r] - M);
+                wsum += f * ml[w * 2 * kMultiMaxRows + kMultiMaxRows + r];
+                acc += f * reinterpret_cast<const float*>(smem + size_t(w) * NST * STAGE)[r * D + d];
+            }
+        }
+        out_row(r)[d] = failed ? NAN : (wsum > 0.f ? acc / wsum : 0.f);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn tensor_map_encoder() {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_acquire);
+    if (f == nullptr) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || ptr == nullptr)
+            return nullptr;
+        f = reinterpret_cast<EncodeTiledFn>(ptr);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+// The cache as a 2D tensor [rows = NB * Hkv * bs][D] bf16, read in boxes of 16 rows x 64
+// elements (128 bytes) with the 128-byte swizzle.
+static bool encode_cache_map(CUtensorMap* map, const void* cache, long long rows, int D) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(D) * 2};
+    const cuuint32_t box[2] = {64, cuuint32_t(kTileTokens)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMultiWarps = 4;
+constexpr int kMultiStages = 2;
+
+template <int D>
+static cudaError_t launch_multi(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p,
+                                cudaStream_t stream) {
+    using Lay = MultiLayout<D, kMultiWarps, kMultiStages>;
+    auto kern = paged_multi_query_kernel<D, kMultiWarps, kMultiStages>;
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit == 0 || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Lay::ALLOC));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const long long grid = (long long)p.num_seqs * p.num_kv_heads;
+    kern<<<unsigned(grid), kMultiWarps * 32, Lay::ALLOC, stream>>>(mk, mv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace pf
+
+using namespace pf;
+
+extern "C" pf_status pf_paged_attention_multi_query(const void* q, const void* k_cache, const void* v_cache,
+                                                    const int32_t* block_tables, const int32_t* context_lens,
+                                                    int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                                    int head_dim, int block_size, int max_blocks_per_seq,
+                                                    int64_t num_blocks, float scale, float* out,
+                                                    pf_stream_t stream) {
+    if (num_seqs < 0 || q_len <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        max_blocks_per_seq <= 0 || num_blocks <= 0 || !std::isfinite(scale) || num_q_heads % num_kv_heads != 0 ||
+        num_blocks > INT32_MAX)
+        return PF_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    if (head_dim != 64 && head_dim != 128) return PF_ERR_UNSUPPORTED;
+    if (block_size % kTileTokens != 0) return PF_ERR_UNSUPPORTED;
+    if ((long long)group * q_len > kMultiMaxRows) return PF_ERR_UNSUPPORTED;
+    const long long rows = num_blocks * num_kv_heads * (long long)block_size;
+    if (rows > INT32_MAX || (long long)num_seqs * num_kv_heads > INT32_MAX) return PF_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PF_OK;
+    auto al = [](const void* ptr, size_t a) { return ptr != nullptr && reinterpret_cast<uintptr_t>(ptr) % a == 0; };
+    if (!al(q, 16) || !al(k_cache, 16) || !al(v_cache, 16) || !al(block_tables, 4) || !al(context_lens, 4) ||
+        !al(out, 16))
+        return PF_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
+    CUtensorMap mk, mv;
+    if (!encode_cache_map(&mk, k_cache, rows, head_dim) || !encode_cache_map(&mv, v_cache, rows, head_dim))
+        return PF_ERR_CUDA;
+    MultiParams p{};
+    p.q = static_cast<const uint16_t*>(q);
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = out;
+    p.err = err;
+    p.num_blocks = num_blocks;
+    p.wait_limit_ns = kDefaultWaitLimitNs;
+    p.scale_log2 = float(double(scale) * 1.4426950408889634);
+    p.num_seqs = num_seqs;
+    p.q_len = q_len;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = group;
+    p.rows = group * q_len;
+    p.block_size = block_size;
+    p.block_shift = (block_size & (block_size - 1)) == 0 ? __builtin_ctz(unsigned(block_size)) : -1;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    const cudaError_t e = head_dim == 64 ? launch_multi<64>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream))
+                                         : launch_multi<128>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
+}
