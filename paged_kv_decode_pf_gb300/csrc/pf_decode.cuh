@@ -198,13 +198,201 @@ __device__ __forceinline__ void load_probs(const float* src, float (&pw)[G]) {
     }
 }
 
+// One warp's share of an item: the lane's slice of the G query rows in fp32
+// registers, the online-softmax state of the head whose scores the lane holds,
+// and the P.V accumulator for D/32 output dims of all G heads.  tile() consumes
+// one 16-token K/V tile from shared memory (nvalid of its rows are tokens).
+template <int D, int G>
+struct WarpAttention {
+    using Geo = DecodeGeometry<D, G>;
+    static constexpr int TT = Geo::TT, LPT = Geo::LPT, TPP = Geo::TPP, NPASS = Geo::NPASS, CPL = Geo::CPL;
+    static constexpr int DUP = Geo::DUP, DPL = Geo::DPL, ROW = Geo::ROW_BYTES;
+
+    int lane, tp, sl, hh, rot;
+    bool writer;  // one lane per (head, token) writes shared state
+    int kofs[CPL];
+    float2 qf[G][CPL][4];
+    float m_run, l_run;
+    float2 acc[G][DPL / 2];
+
+    __device__ __forceinline__ void init(int lane_) {
+        lane = lane_;
+        tp = lane / LPT;
+        sl = lane % LPT;
+        hh = sl / DUP;
+        rot = tp % Geo::ROT_MOD;
+        writer = (sl % DUP) == 0;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) kofs[j] = tp * ROW + (sl + LPT * ((j + rot) % CPL)) * 16;
+    }
+
+    // q rows of the group's G heads, consecutive [G][D] bf16
+    __device__ __forceinline__ void load_q(const uint16_t* qrows) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                const int chunk = sl + LPT * ((j + rot) % CPL);
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(qrows + h * D + chunk * 8));
+                qf[h][j][0] = bf16x2_to_float2(w.x);
+                qf[h][j][1] = bf16x2_to_float2(w.y);
+                qf[h][j][2] = bf16x2_to_float2(w.z);
+                qf[h][j][3] = bf16x2_to_float2(w.w);
+            }
+        }
+    }
+
+    __device__ __forceinline__ void reset() {
+        m_run = -INFINITY;
+        l_run = 0.f;
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < DPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
+    }
+
+    __device__ __forceinline__ void tile(const unsigned char* Ks, const unsigned char* Vs, int nvalid, float* psm,
+                                         float scale_log2) {
+        // -- scores of this lane's tokens for head hh, base-2 units
+        float sc[NPASS];
+#pragma unroll
+        for (int pass = 0; pass < NPASS; ++pass) {
+            const unsigned char* rowp = Ks + pass * TPP * ROW;
+            float2 a[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) a[h] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                const uint4 w = *reinterpret_cast<const uint4*>(rowp + kofs[j]);
+                const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
+                const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    a[h] = ffma2(qf[h][j][0], k0, a[h]);
+                    a[h] = ffma2(qf[h][j][1], k1, a[h]);
+                    a[h] = ffma2(qf[h][j][2], k2, a[h]);
+                    a[h] = ffma2(qf[h][j][3], k3, a[h]);
+                }
+            }
+            float v[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) v[h] = a[h].x + a[h].y;
+            const float dot = reduce_scatter_heads<G, LPT>(v, sl);
+            sc[pass] = (pass * TPP + tp < nvalid) ? dot * scale_log2 : -INFINITY;
+        }
+
+        // -- online softmax for head hh
+        float mx = sc[0];
+#pragma unroll
+        for (int pass = 1; pass < NPASS; ++pass) mx = fmaxf(mx, sc[pass]);
+#pragma unroll
+        for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, o));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = exp2_approx(m_run - m_new);
+        float psum = 0.f;
+#pragma unroll
+        for (int pass = 0; pass < NPASS; ++pass) {
+            const float pv = exp2_approx(sc[pass] - m_new);
+            psum += pv;
+            if (writer) psm[(pass * TPP + tp) * G + hh] = pv;
+        }
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+        if (writer && tp == 0) psm[TT * G + hh] = alpha;
+        __syncwarp();
+
+        // -- acc = alpha * acc + sum_t p_t V_t, lane owns dims [lane*DPL, lane*DPL + DPL)
+        {
+            float al[G];
+            load_probs<G>(psm + TT * G, al);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < DPL / 2; ++e) {
+                    acc[h][e].x *= al[h];
+                    acc[h][e].y *= al[h];
+                }
+        }
+        auto pv_step = [&](int t) {
+            float pw[G];
+            load_probs<G>(psm + t * G, pw);
+            float2 vv[DPL / 2];
+            if constexpr (DPL == 4) {
+                const uint2 w = *reinterpret_cast<const uint2*>(Vs + t * ROW + lane * 8);
+                vv[0] = bf16x2_to_float2(w.x);
+                vv[1] = bf16x2_to_float2(w.y);
+            } else {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + t * ROW + lane * 4);
+                vv[0] = bf16x2_to_float2(w);
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < DPL / 2; ++e) acc[h][e] = ffma2(make_float2(pw[h], pw[h]), vv[e], acc[h][e]);
+        };
+        if (nvalid == TT) {
+#pragma unroll
+            for (int t = 0; t < TT; ++t) pv_step(t);
+        } else {
+            for (int t = 0; t < nvalid; ++t) pv_step(t);  // rows past the length are never read
+        }
+        __syncwarp();
+    }
+
+    // Per-head l over the lanes holding that head, then (m, l) of the G heads to
+    // ml[0 .. 2G) and acc to accs [G][D] (fp32).
+    __device__ __forceinline__ void stash(float* ml, float* accs) {
+#pragma unroll
+        for (int o = LPT; o < 32; o <<= 1) l_run += __shfl_xor_sync(FULL_MASK, l_run, o);
+        __syncwarp();
+        if (writer && tp == 0) {
+            ml[hh] = m_run;
+            ml[G + hh] = l_run;
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < DPL / 2; ++e)
+                *reinterpret_cast<float2*>(accs + h * D + lane * DPL + 2 * e) = acc[h][e];
+    }
+};
+
+// Merge the NW warps' stashes of one item and write it: element e = h * D + d of the
+// group; ml(w) / accs(w) locate warp w's (m, l) pairs and [G][D] accumulator.  Writes
+// out_rows[h * D + d] (normalised), and for a partition its natural-log max and sum.
+template <int D, int G, int NW, typename MlFn, typename AccFn>
+__device__ __forceinline__ void merge_warps_and_store(MlFn ml, AccFn accs, bool failed, float* out_rows,
+                                                      float* part_m, float* part_l, size_t part_stride) {
+    for (int e = threadIdx.x; e < G * D; e += NW * 32) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, ml(w)[h]);
+        float wsum = 0.f, o = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float f = exp2_approx(ml(w)[h] - M);
+                wsum += f * ml(w)[G + h];
+                o += f * accs(w)[h * D + d];
+            }
+        }
+        float res = wsum > 0.f ? o / wsum : 0.f;
+        if (failed) res = NAN;
+        out_rows[h * part_stride * D + d] = res;
+        if (part_m != nullptr && d == 0) {
+            part_m[h * part_stride] = failed ? NAN : M * 0.6931471805599453f;
+            part_l[h * part_stride] = failed ? NAN : wsum;
+        }
+    }
+}
+
 template <int D, int G, int NW, int NST, int MODE>
 __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParams p) {
     constexpr bool PART = MODE == MODE_PARTITION;
     constexpr bool APPEND = MODE == MODE_DECODE_APPEND;
     using Geo = DecodeGeometry<D, G>;
-    constexpr int TT = Geo::TT, LPT = Geo::LPT, TPP = Geo::TPP, NPASS = Geo::NPASS, CPL = Geo::CPL;
-    constexpr int DUP = Geo::DUP, DPL = Geo::DPL, ROW = Geo::ROW_BYTES, TILE = Geo::TILE_BYTES;
+    constexpr int TT = Geo::TT, ROW = Geo::ROW_BYTES, TILE = Geo::TILE_BYTES;
     constexpr int PSM_PAD = Geo::PSM_PAD;
     constexpr int R = NST + 2;  // table entries lane 0 holds ahead of the copies
 
@@ -214,10 +402,6 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(flags) + flag_bytes<NW>());
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tp = lane / LPT, sl = lane % LPT;
-    const int hh = sl / DUP;                 // head (within the group) of this lane's scores
-    const int rot = tp % Geo::ROT_MOD;
-    const bool writer = (sl % DUP) == 0;     // one lane per (head, token) writes shared state
 
     // ---- which item
     int seq, kvh, part = 0;
@@ -336,31 +520,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         }
     }
 
-    // ---- this lane's slice of the G query rows, fp32, in its chunk-read order
-    float2 qf[G][CPL][4];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const uint16_t* qrow = p.q + (size_t(seq) * Hq + qh0 + h) * D;
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const int chunk = sl + LPT * ((j + rot) % CPL);
-            const uint4 w = __ldg(reinterpret_cast<const uint4*>(qrow + chunk * 8));
-            qf[h][j][0] = bf16x2_to_float2(w.x);
-            qf[h][j][1] = bf16x2_to_float2(w.y);
-            qf[h][j][2] = bf16x2_to_float2(w.z);
-            qf[h][j][3] = bf16x2_to_float2(w.w);
-        }
-    }
-    int kofs[CPL];
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) kofs[j] = tp * ROW + (sl + LPT * ((j + rot) % CPL)) * 16;
-
-    float m_run = -INFINITY, l_run = 0.f;
-    float2 acc[G][DPL / 2];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < DPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
+    // ---- this lane's slice of the G query rows and the softmax / P.V state
+    WarpAttention<D, G> wa;
+    wa.init(lane);
+    wa.load_q(p.q + (size_t(seq) * Hq + qh0) * D);
+    wa.reset();
 
     bool timed_out = false;
     int k = 0;
@@ -399,90 +563,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
             }
         }
 
-        // -- scores of this lane's tokens for head hh, base-2 units
-        float sc[NPASS];
-#pragma unroll
-        for (int pass = 0; pass < NPASS; ++pass) {
-            const unsigned char* rowp = Ks + pass * TPP * ROW;
-            float2 a[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) a[h] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                const uint4 w = *reinterpret_cast<const uint4*>(rowp + kofs[j]);
-                const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
-                const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    a[h] = ffma2(qf[h][j][0], k0, a[h]);
-                    a[h] = ffma2(qf[h][j][1], k1, a[h]);
-                    a[h] = ffma2(qf[h][j][2], k2, a[h]);
-                    a[h] = ffma2(qf[h][j][3], k3, a[h]);
-                }
-            }
-            float v[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) v[h] = a[h].x + a[h].y;
-            const float dot = reduce_scatter_heads<G, LPT>(v, sl);
-            sc[pass] = (pass * TPP + tp < nvalid) ? dot * p.scale_log2 : -INFINITY;
-        }
-
-        // -- online softmax for head hh
-        float mx = sc[0];
-#pragma unroll
-        for (int pass = 1; pass < NPASS; ++pass) mx = fmaxf(mx, sc[pass]);
-#pragma unroll
-        for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, o));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = exp2_approx(m_run - m_new);
-        float psum = 0.f;
-#pragma unroll
-        for (int pass = 0; pass < NPASS; ++pass) {
-            const float pv = exp2_approx(sc[pass] - m_new);
-            psum += pv;
-            if (writer) psm[(pass * TPP + tp) * G + hh] = pv;
-        }
-        l_run = l_run * alpha + psum;
-        m_run = m_new;
-        if (writer && tp == 0) psm[TT * G + hh] = alpha;
-        __syncwarp();
-
-        // -- acc = alpha * acc + sum_t p_t V_t, lane owns dims [lane*DPL, lane*DPL + DPL)
-        {
-            float al[G];
-            load_probs<G>(psm + TT * G, al);
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < DPL / 2; ++e) {
-                    acc[h][e].x *= al[h];
-                    acc[h][e].y *= al[h];
-                }
-        }
-        auto pv_step = [&](int t) {
-            float pw[G];
-            load_probs<G>(psm + t * G, pw);
-            float2 vv[DPL / 2];
-            if constexpr (DPL == 4) {
-                const uint2 w = *reinterpret_cast<const uint2*>(Vs + t * ROW + lane * 8);
-                vv[0] = bf16x2_to_float2(w.x);
-                vv[1] = bf16x2_to_float2(w.y);
-            } else {
-                const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + t * ROW + lane * 4);
-                vv[0] = bf16x2_to_float2(w);
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < DPL / 2; ++e) acc[h][e] = ffma2(make_float2(pw[h], pw[h]), vv[e], acc[h][e]);
-        };
-        if (nvalid == TT) {
-#pragma unroll
-            for (int t = 0; t < TT; ++t) pv_step(t);
-        } else {
-            for (int t = 0; t < nvalid; ++t) pv_step(t);  // rows past the length are never read
-        }
-        __syncwarp();
+        wa.tile(Ks, Vs, nvalid, psm, p.scale_log2);
 
         // -- refill the stage just drained
         if (lane == 0 && k + NST < nk) {
@@ -501,22 +582,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     if (lane == 0 && bad_block) set_error(p.err, ERR_BOUNDS);
     const bool warp_failed = __any_sync(FULL_MASK, bad_block || timed_out);
 
-    // ---- per-head sum of l over the lanes holding that head
-#pragma unroll
-    for (int o = LPT; o < 32; o <<= 1) l_run += __shfl_xor_sync(FULL_MASK, l_run, o);
-
     // ---- stash (m, l, acc) of this warp; its stage memory and psm are free now
-    __syncwarp();
-    if (writer && tp == 0) {
-        psm[hh] = m_run;
-        psm[G + hh] = l_run;
-    }
-    float* accs = reinterpret_cast<float*>(my_stages);
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < DPL / 2; ++e)
-            *reinterpret_cast<float2*>(accs + h * D + lane * DPL + 2 * e) = acc[h][e];
+    wa.stash(psm, reinterpret_cast<float*>(my_stages));
     if (lane == 0) flags[warp] = warp_failed ? 1 : 0;
     __syncthreads();
 
@@ -524,33 +591,15 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     bool failed = false;
 #pragma unroll
     for (int w = 0; w < NW; ++w) failed = failed || flags[w] != 0;
-    for (int e = threadIdx.x; e < G * D; e += NW * 32) {
-        const int h = e / D, d = e % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, psm_all[w * PSM_PAD + h]);
-        float wsum = 0.f, o = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float f = exp2_approx(psm_all[w * PSM_PAD + h] - M);
-                const float* accw = reinterpret_cast<const float*>(smem + size_t(w) * NST * 2 * TILE);
-                wsum += f * psm_all[w * PSM_PAD + G + h];
-                o += f * accw[h * D + d];
-            }
-        }
-        float res = wsum > 0.f ? o / wsum : 0.f;
-        if (failed) res = NAN;
-        if constexpr (PART) {
-            const size_t slot = (size_t(seq) * Hq + qh0 + h) * p.num_partitions + part;
-            p.out[slot * D + d] = res;
-            if (d == 0) {
-                p.part_m[slot] = failed ? NAN : M * 0.6931471805599453f;
-                p.part_l[slot] = failed ? NAN : wsum;
-            }
-        } else {
-            p.out[(size_t(seq) * Hq + qh0) * D + e] = res;
-        }
+    auto ml_of = [&](int w) { return psm_all + w * PSM_PAD; };
+    auto acc_of = [&](int w) { return reinterpret_cast<const float*>(smem + size_t(w) * NST * 2 * TILE); };
+    if constexpr (PART) {
+        const size_t slot0 = (size_t(seq) * Hq + qh0) * p.num_partitions + part;
+        merge_warps_and_store<D, G, NW>(ml_of, acc_of, failed, p.out + slot0 * D, p.part_m + slot0,
+                                        p.part_l + slot0, size_t(p.num_partitions));
+    } else {
+        merge_warps_and_store<D, G, NW>(ml_of, acc_of, failed, p.out + (size_t(seq) * Hq + qh0) * D, nullptr,
+                                        nullptr, 1);
     }
 }
 
@@ -576,27 +625,6 @@ cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream) {
     if (grid <= 0) return cudaSuccess;
     kern<<<unsigned(grid), NW * 32, smem, stream>>>(p);
     return cudaGetLastError();
-}
-
-template <int D, int G, int NW, int NST>
-cudaError_t launch_decode_mode(const DecodeParams& p, int mode, cudaStream_t stream) {
-    switch (mode) {
-        case MODE_DECODE: return launch_decode_variant<D, G, NW, NST, MODE_DECODE>(p, stream);
-        case MODE_PARTITION: return launch_decode_variant<D, G, NW, NST, MODE_PARTITION>(p, stream);
-        case MODE_DECODE_APPEND: return launch_decode_variant<D, G, NW, NST, MODE_DECODE_APPEND>(p, stream);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-template <int D, int NW, int NST>
-cudaError_t launch_decode_for_dim(const DecodeParams& p, int group, int mode, cudaStream_t stream) {
-    switch (group) {
-        case 1: return launch_decode_mode<D, 1, NW, NST>(p, mode, stream);
-        case 2: return launch_decode_mode<D, 2, NW, NST>(p, mode, stream);
-        case 4: return launch_decode_mode<D, 4, NW, NST>(p, mode, stream);
-        case 8: return launch_decode_mode<D, 8, NW, NST>(p, mode, stream);
-        default: return cudaErrorInvalidValue;
-    }
 }
 
 }  // namespace pf

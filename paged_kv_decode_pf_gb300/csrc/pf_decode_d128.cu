@@ -1,6 +1,6 @@
 // head_dim = 128 instantiations of the decode / partition kernel:
 // 4 warps per CTA, 2 stages of 16-token K+V tiles (8 KiB) per warp, three CTAs per SM.
-#include "pf_decode.cuh"
+#include "pf_partition.cuh"
 
 // Warps per CTA and stages per warp (compile-time tunables).
 #ifndef PF_D128_WARPS

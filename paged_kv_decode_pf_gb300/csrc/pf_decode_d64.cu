@@ -1,6 +1,6 @@
 // head_dim = 64 instantiations of the decode / partition kernel:
 // 4 warps per CTA, 4 stages of 16-token K+V tiles (4 KiB) per warp.
-#include "pf_decode.cuh"
+#include "pf_partition.cuh"
 
 // Warps per CTA and stages per warp (compile-time tunables).
 #ifndef PF_D64_WARPS
