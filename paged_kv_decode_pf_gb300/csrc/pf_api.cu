@@ -120,14 +120,29 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) lse_merge_kernel(const float
     const int np = (active && !bad) ? (L + partition_size - 1) / partition_size : 0;
     const size_t base = active ? size_t(row) * num_partitions : 0;
 
-    float M = -INFINITY;
-    for (int k = lane; k < np; k += 32) M = fmaxf(M, tmp_m[base + k]);
+    // The partials come from the partition pass launched just before on this stream;
+    // with programmatic launch this CTA may start early and waits here for that grid.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // maximum M and weight sum W = sum_k l_k exp(m_k - M) in one online pass per lane ...
+    float M = -INFINITY, W = 0.f;
+    for (int k = lane; k < np; k += 32) {
+        const float m = tmp_m[base + k], l = tmp_l[base + k];
+        if (m > M) {
+            W = W * exp2_approx((M - m) * kLog2e) + l;
+            M = m;
+        } else {
+            W += l * exp2_approx((m - M) * kLog2e);
+        }
+    }
+    // ... then across the warp
 #pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, s));
-    float W = 0.f;
-    for (int k = lane; k < np; k += 32) W += tmp_l[base + k] * exp2_approx((tmp_m[base + k] - M) * kLog2e);
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) W += __shfl_xor_sync(FULL_MASK, W, s);
+    for (int s = 16; s >= 1; s >>= 1) {
+        const float M2 = __shfl_xor_sync(FULL_MASK, M, s), W2 = __shfl_xor_sync(FULL_MASK, W, s);
+        const float Mn = fmaxf(M, M2);
+        if (Mn != -INFINITY) W = W * exp2_approx((M - Mn) * kLog2e) + W2 * exp2_approx((M2 - Mn) * kLog2e);
+        M = Mn;
+    }
 
     float acc[DPL];
 #pragma unroll
@@ -142,7 +157,7 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) lse_merge_kernel(const float
             x[0] = v.x; x[1] = v.y;
         }
     };
-    constexpr int BATCH = 8;  // partitions whose loads are in flight together
+    constexpr int BATCH = 16;  // partitions whose loads are in flight together
     int k = sub;
     for (; k + (BATCH - 1) * WPR < np; k += BATCH * WPR) {
         float mk[BATCH], lk[BATCH], x[BATCH][DPL];
@@ -179,19 +194,39 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) lse_merge_kernel(const float
     }
 }
 
+// Launched with programmatic stream serialization: the merge's CTAs may be
+// scheduled while the partition pass finishes, and wait in griddepcontrol.wait.
+template <int D, int WPR>
+static cudaError_t launch_merge_wpr(unsigned blocks, cudaStream_t s, const float* to, const float* tm,
+                                    const float* tl, const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                    int partition_size, int np, int max_context_len, float* out, unsigned* err) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(MERGE_WARPS * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<D, WPR>, to, tm, tl, context_lens, num_seqs, num_q_heads,
+                              partition_size, np, max_context_len, out, err);
+}
+
 template <int D>
-static void launch_merge(int wpr, unsigned blocks, cudaStream_t s, const float* to, const float* tm, const float* tl,
-                         const int32_t* context_lens, int num_seqs, int num_q_heads, int partition_size, int np,
-                         int max_context_len, float* out, unsigned* err) {
+static cudaError_t launch_merge(int wpr, unsigned blocks, cudaStream_t s, const float* to, const float* tm,
+                                const float* tl, const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                int partition_size, int np, int max_context_len, float* out, unsigned* err) {
     switch (wpr) {
-        case 1: lse_merge_kernel<D, 1><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs,
-                    num_q_heads, partition_size, np, max_context_len, out, err); break;
-        case 2: lse_merge_kernel<D, 2><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs,
-                    num_q_heads, partition_size, np, max_context_len, out, err); break;
-        case 4: lse_merge_kernel<D, 4><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs,
-                    num_q_heads, partition_size, np, max_context_len, out, err); break;
-        default: lse_merge_kernel<D, 8><<<blocks, MERGE_WARPS * 32, 0, s>>>(to, tm, tl, context_lens, num_seqs,
-                    num_q_heads, partition_size, np, max_context_len, out, err); break;
+        case 1: return launch_merge_wpr<D, 1>(blocks, s, to, tm, tl, context_lens, num_seqs, num_q_heads,
+                                              partition_size, np, max_context_len, out, err);
+        case 2: return launch_merge_wpr<D, 2>(blocks, s, to, tm, tl, context_lens, num_seqs, num_q_heads,
+                                              partition_size, np, max_context_len, out, err);
+        case 4: return launch_merge_wpr<D, 4>(blocks, s, to, tm, tl, context_lens, num_seqs, num_q_heads,
+                                              partition_size, np, max_context_len, out, err);
+        default: return launch_merge_wpr<D, 8>(blocks, s, to, tm, tl, context_lens, num_seqs, num_q_heads,
+                                               partition_size, np, max_context_len, out, err);
     }
 }
 
@@ -463,13 +498,12 @@ pf_status pf_paged_attention_merge(const void* workspace, const int32_t* context
     const float* to = reinterpret_cast<const float*>(ws + off_o);
     const float* tm = reinterpret_cast<const float*>(ws + off_m);
     const float* tl = reinterpret_cast<const float*>(ws + off_l);
-    if (head_dim == 64)
-        launch_merge<64>(wpr, unsigned(blocks), s, to, tm, tl, context_lens, num_seqs, num_q_heads, partition_size,
-                         np, max_context_len, out, err);
-    else
-        launch_merge<128>(wpr, unsigned(blocks), s, to, tm, tl, context_lens, num_seqs, num_q_heads, partition_size,
-                          np, max_context_len, out, err);
-    return cudaGetLastError() == cudaSuccess ? PF_OK : PF_ERR_CUDA;
+    const cudaError_t e =
+        head_dim == 64 ? launch_merge<64>(wpr, unsigned(blocks), s, to, tm, tl, context_lens, num_seqs, num_q_heads,
+                                          partition_size, np, max_context_len, out, err)
+                       : launch_merge<128>(wpr, unsigned(blocks), s, to, tm, tl, context_lens, num_seqs, num_q_heads,
+                                           partition_size, np, max_context_len, out, err);
+    return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }
 
 pf_status pf_get_device_error(pf_stream_t stream) {

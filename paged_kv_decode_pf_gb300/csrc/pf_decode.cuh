@@ -402,6 +402,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(flags) + flag_bytes<NW>());
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if constexpr (PART) asm volatile("griddepcontrol.launch_dependents;");  // the merge waits for completion
 
     // ---- which item
     int seq, kvh, part = 0;

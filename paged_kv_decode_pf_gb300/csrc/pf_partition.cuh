@@ -118,6 +118,9 @@ __global__ void __launch_bounds__(NW * 32) paged_partition_persistent_kernel(con
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::BARS);
     int* keys = reinterpret_cast<int*>(smem + Lay::KEYS);
 
+    // The merge that follows may be scheduled as SMs drain; it waits for this grid to complete.
+    asm volatile("griddepcontrol.launch_dependents;");
+
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
     const int U = partition_prefix<NW>(p, keys) * Hkv;
