@@ -43,6 +43,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 DECODE_SOURCES = ["paged_kv_decode_pf_gb300/csrc/pf_decode.cuh", "paged_kv_decode_pf_gb300/csrc/pf_device.cuh",
+                  "paged_kv_decode_pf_gb300/csrc/pf_internal.h",
                   "paged_kv_decode_pf_gb300/csrc/pf_decode_d128.cu", "paged_kv_decode_pf_gb300/csrc/pf_decode_d64.cu"]
 
 
@@ -570,6 +571,10 @@ def main():
         cpu = {"value": round(sb / secs / 1e9, 4), "unit": "GB/s", "cores": orc.max_threads(), "kind": "oracle",
                "sample": desc, "seconds": round(secs, 3),
                "seq_steps_per_s": round(n / secs, 3)}
+        secs1, sb1, n1, desc1 = oracle_sample_run(orc, wl, min(args.oracle_seconds, 5.0), threads=1)
+        cpu["single_thread"] = {"value": round(sb1 / secs1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                "sample": desc1, "seconds": round(secs1, 3),
+                                "seq_steps_per_s": round(n1 / secs1, 3)}
 
     if rank == 0:
         clocks = sampler.summary()
