@@ -97,6 +97,27 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __r
 // before the accumulation.  WPR grows with the partition count (host side).
 constexpr int MERGE_WARPS = 8;
 
+// Loads of the partials the partition pass wrote just before: each is read once.
+__device__ __forceinline__ float ld_stream(const float* p) {
+    float v;
+    asm volatile("ld.global.cs.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+template <int DPL>
+__device__ __forceinline__ void ld_stream_row(const float* src, bool in, float (&x)[DPL]) {
+    if constexpr (DPL == 4) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (in)
+            asm volatile("ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(src));
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+        float2 v = make_float2(0.f, 0.f);
+        if (in) asm volatile("ld.global.cs.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(src));
+        x[0] = v.x; x[1] = v.y;
+    }
+}
+
 template <int D, int WPR>
 __global__ void __launch_bounds__(MERGE_WARPS * 32) lse_merge_kernel(const float* __restrict__ tmp_out,
                                                                      const float* __restrict__ tmp_m,
@@ -124,15 +145,23 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) lse_merge_kernel(const float
     // with programmatic launch this CTA may start early and waits here for that grid.
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // maximum M and weight sum W = sum_k l_k exp(m_k - M) in one online pass per lane ...
+    // maximum M and weight sum W = sum_k l_k exp(m_k - M), online per lane over batches
+    // of SB partitions whose loads are all in flight together ...
+    constexpr int SB = 8;
     float M = -INFINITY, W = 0.f;
-    for (int k = lane; k < np; k += 32) {
-        const float m = tmp_m[base + k], l = tmp_l[base + k];
-        if (m > M) {
-            W = W * exp2_approx((M - m) * kLog2e) + l;
-            M = m;
-        } else {
-            W += l * exp2_approx((m - M) * kLog2e);
+    for (int k0 = 0; k0 < np; k0 += 32 * SB) {
+        float mk[SB], lk[SB];
+#pragma unroll
+        for (int u = 0; u < SB; ++u) {
+            const int k = k0 + lane + 32 * u;
+            mk[u] = k < np ? ld_stream(tmp_m + base + k) : -INFINITY;
+            lk[u] = k < np ? ld_stream(tmp_l + base + k) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < SB; ++u) {
+            const float Mn = fmaxf(M, mk[u]);
+            if (Mn != -INFINITY) W = W * exp2_approx((M - Mn) * kLog2e) + lk[u] * exp2_approx((mk[u] - Mn) * kLog2e);
+            M = Mn;
         }
     }
     // ... then across the warp
@@ -144,42 +173,26 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) lse_merge_kernel(const float
         M = Mn;
     }
 
+    // weighted sum of this warp's partitions sub, sub + WPR, ..., AB at a time
     float acc[DPL];
 #pragma unroll
     for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-    auto load_row = [&](int k, float (&x)[DPL]) {
-        const float* src = tmp_out + (base + k) * D + lane * DPL;
-        if constexpr (DPL == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src);
-            x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-        } else {
-            const float2 v = *reinterpret_cast<const float2*>(src);
-            x[0] = v.x; x[1] = v.y;
-        }
-    };
-    constexpr int BATCH = 16;  // partitions whose loads are in flight together
-    int k = sub;
-    for (; k + (BATCH - 1) * WPR < np; k += BATCH * WPR) {
-        float mk[BATCH], lk[BATCH], x[BATCH][DPL];
+    constexpr int AB = 16;
+    for (int k0 = sub; k0 < np; k0 += AB * WPR) {
+        float wk[AB], x[AB][DPL];
 #pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            mk[u] = tmp_m[base + k + u * WPR];
-            lk[u] = tmp_l[base + k + u * WPR];
-            load_row(k + u * WPR, x[u]);
+        for (int u = 0; u < AB; ++u) {
+            const int k = k0 + u * WPR;
+            const bool in = k < np;
+            const float m = in ? ld_stream(tmp_m + base + k) : -INFINITY;
+            const float l = in ? ld_stream(tmp_l + base + k) : 0.f;
+            wk[u] = in ? l * exp2_approx((m - M) * kLog2e) : 0.f;
+            ld_stream_row(tmp_out + (base + (in ? k : 0)) * D + lane * DPL, in, x[u]);
         }
 #pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            const float w = lk[u] * exp2_approx((mk[u] - M) * kLog2e);
+        for (int u = 0; u < AB; ++u)
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[e] += w * x[u][e];
-        }
-    }
-    for (; k < np; k += WPR) {
-        float x[DPL];
-        load_row(k, x);
-        const float w = tmp_l[base + k] * exp2_approx((tmp_m[base + k] - M) * kLog2e);
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[e] += w * x[e];
+            for (int e = 0; e < DPL; ++e) acc[e] += wk[u] * x[u][e];
     }
 #pragma unroll
     for (int e = 0; e < DPL; ++e) accs[warp][lane * DPL + e] = acc[e];

@@ -430,22 +430,24 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         t1 = min(L, t0 + p.partition_size);
     }
     // Decode with append: the new token of this sequence is its position L-1, and its
-    // slot must be that position's slot (or -1: nothing to append).  app_row is the
-    // token's row in the cache, [block][kv head][offset], or -1.
-    long long app_row = -1;
+    // slot must be that position's slot (or -1: nothing to append).  The slot and the
+    // last table entry are loaded here but checked only where they are used -- when the
+    // tile holding position L-1 lands and at the end -- so their latency does not delay
+    // the first copies.  A mismatch writes nothing and NaN-fills the rows.
+    long long app_slot = -1;
+    int app_blk = -1;
     if constexpr (APPEND) {
-        const long long slot = __ldg(p.slot_mapping + seq);
-        if (!len_bad && slot != -1) {
-            bool ok = L >= 1;
-            if (ok) {
-                const int blk = __ldg(p.block_tables + size_t(seq) * p.max_blocks_per_seq + (L - 1) / p.block_size);
-                ok = blk >= 0 && (long long)blk < p.num_blocks &&
-                     slot == (long long)blk * p.block_size + (L - 1) % p.block_size;
-            }
-            if (ok) app_row = ((slot / p.block_size) * p.num_kv_heads + kvh) * p.block_size + slot % p.block_size;
-            else len_bad = true;  // nothing is written for this sequence
-        }
+        app_slot = __ldg(p.slot_mapping + seq);
+        if (!len_bad && L >= 1)
+            app_blk = __ldg(p.block_tables + size_t(seq) * p.max_blocks_per_seq + (L - 1) / p.block_size);
     }
+    auto append_row = [&]() -> long long {  // the new token's cache row [block][kv head][offset], -1, or -2 (bad)
+        if (app_slot == -1) return -1;
+        const bool ok = L >= 1 && app_blk >= 0 && (long long)app_blk < p.num_blocks &&
+                        app_slot == (long long)app_blk * p.block_size + (L - 1) % p.block_size;
+        return ok ? ((app_slot / p.block_size) * p.num_kv_heads + kvh) * p.block_size + app_slot % p.block_size
+                  : -2;
+    };
     if (len_bad) {
         if (threadIdx.x == 0) set_error(p.err, ERR_BOUNDS);
         for (int e = threadIdx.x; e < G * D; e += NW * 32) {
@@ -538,7 +540,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         const int nvalid = min(TT, t1 - tile_token(k));
         if constexpr (APPEND) {
             const int r = (L - 1) - tile_token(k);
-            if (app_row >= 0 && r >= 0 && r < TT) {
+            const long long app_row = (r >= 0 && r < TT) ? append_row() : -1;
+            if (app_row >= 0) {
                 // The tile holding the new token: its copy brought the slot's old bytes.
                 // Put the new K/V row in their place, and write it to the cache.
                 constexpr int LB = ROW / 32;  // bytes of the row per lane
@@ -579,6 +582,9 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         if (lane == 0) set_error(p.err, ERR_TIMEOUT);
         const int last = min(k + NST, nk);
         for (int kk = k; kk < last; ++kk) mbar_wait_bounded(bar0 + 8 * (kk % NST), (kk / NST) & 1, p.wait_limit_ns);
+    }
+    if constexpr (APPEND) {
+        if (append_row() == -2) bad_block = true;  // the slot is not position L-1's: nothing was written
     }
     if (lane == 0 && bad_block) set_error(p.err, ERR_BOUNDS);
     const bool warp_failed = __any_sync(FULL_MASK, bad_block || timed_out);

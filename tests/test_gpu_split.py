@@ -70,3 +70,14 @@ def test_workspace_too_small_is_rejected(pf):
     with pytest.raises(pf.PFError) as e:
         pf.paged_attention_decode_partition(*attn_args(d), 32, 70, ws)
     assert e.value.status == pf.PF_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_merge_many_partitions(pf, oracle_lib, D):
+    """More partitions per row than one batch of the merge's loads (313 at P=16): the
+    statistics and the weighted sums run over several batches with a ragged last one."""
+    wl = make_workload("manyparts", 4, 8, 2, D, 16, [5000, 4097, 16, 1], seed=44 + D)
+    d = to_device(wl)
+    got, _, _ = split(pf, d, wl, 16)
+    ref = oracle_lib.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    check_close(got, ref)
