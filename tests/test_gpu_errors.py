@@ -46,6 +46,21 @@ def test_split_length_beyond_workspace_flags_bounds(pf):
     assert np.isfinite(out[0]).all() and np.isnan(out[1]).all()
 
 
+def test_split_bad_block_id_flags_bounds(pf, oracle_lib):
+    """The persistent partition pass meets a table entry outside the pool: that partition's
+    partial is NaN, the merge carries it into the sequence's rows, and the word is set."""
+    wl = make_workload("badblks", 3, 8, 2, 128, 16, [40, 50, 60], seed=54, pool_scale=2)
+    ref = oracle_lib.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    d = to_device(wl)
+    d["block_tables"][1, 2] = wl.num_blocks            # seq 1, tokens 32..47
+    ws = pf.alloc_workspace(3, 8, 128, 64, 32, "cuda")
+    pf.paged_attention_decode_partition(*attn_args(d), 32, 64, ws)
+    out = pf.paged_attention_merge(ws, d["context_lens"], 8, 128, 32, 64).cpu().numpy()
+    assert pf.get_device_error() == pf.PF_ERR_DEVICE_BOUNDS
+    assert np.isnan(out[1]).all()
+    check_close(out[[0, 2]], ref[[0, 2]])
+
+
 def test_bounded_wait_times_out_and_context_survives(pf):
     torch.cuda.synchronize()
     assert pf.get_device_error() == pf.PF_OK
