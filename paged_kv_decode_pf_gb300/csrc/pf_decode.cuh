@@ -377,7 +377,7 @@ __device__ __forceinline__ void merge_warps_and_store(MlFn ml, AccFn accs, bool 
                 o += f * accs(w)[h * D + d];
             }
         }
-        float res = wsum > 0.f ? o / wsum : 0.f;
+        float res = wsum == 0.f ? 0.f : o / wsum;  // no token: 0; a NaN input stays NaN
         if (failed) res = NAN;
         out_rows[h * part_stride * D + d] = res;
         if (part_m != nullptr && d == 0) {

@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(NW * 32) paged_multi_query_kernel(const __grid
                 acc += f * reinterpret_cast<const float*>(smem + size_t(w) * NST * STAGE)[r * D + d];
             }
         }
-        out_row(r)[d] = failed ? NAN : (wsum > 0.f ? acc / wsum : 0.f);
+        out_row(r)[d] = failed ? NAN : (wsum == 0.f ? 0.f : acc / wsum);  // a NaN input stays NaN
     }
 }
 

@@ -118,9 +118,10 @@ def test_block_permutation_gives_bit_identical_output(pf, config_workload):
 
 def test_deterministic(pf, config_workload):
     d = to_device(config_workload(3))
+    pf.reshape_and_cache(d["new_k"], d["new_v"], d["slot_mapping"], d["k_cache"], d["v_cache"])
     a = decode(pf, d)
     b = decode(pf, d)
-    assert np.array_equal(a, b)
+    assert np.all(np.isfinite(a)) and np.array_equal(a, b)
 
 
 def test_poison_is_never_read(pf, oracle_lib):
@@ -137,6 +138,25 @@ def test_poison_is_never_read(pf, oracle_lib):
     expect = np.zeros_like(bad)
     expect[3, 4:8] = True
     assert np.array_equal(bad, expect)
+    b = wl.block_tables[1, 0]
+    wl.k_cache[b, 0, 7, :] = BF16_NAN                        # seq 1, kv head 0, token 7: a NaN score
+    got3 = decode(pf, to_device(wl))
+    bad = ~np.isfinite(got3).all(axis=2)
+    expect[1, 0:4] = True
+    assert np.array_equal(bad, expect)
+    assert np.isnan(got3[1, 0:4]).all()                       # NaN, not a silent zero
+
+
+def test_nan_key_in_the_decode_without_its_append(pf, oracle_lib, config_workload):
+    """The continuous-batch cache before its append holds NaN in every slot about to be
+    filled (position L-1 of 56 sequences): those rows are NaN, as in the oracle."""
+    wl = config_workload(3)
+    got = decode(pf, to_device(wl))
+    ref = oracle_out(oracle_lib, wl)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    rows = ~np.isnan(ref).any(axis=(1, 2))
+    assert rows.sum() == 8                                     # the 8 sequences that append nothing
+    check_close(got[rows], ref[rows])
 
 
 def test_scale_argument(pf, oracle_lib):

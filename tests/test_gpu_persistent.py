@@ -10,7 +10,9 @@ import numpy as np
 import pytest
 import torch
 
-from tests.helpers import attn_args, check_close, to_device
+import dataclasses
+
+from tests.helpers import attn_args, check_close, numpy_scatter, to_device
 from workloads import make_workload
 
 pytestmark = pytest.mark.gpu
@@ -32,6 +34,17 @@ def oracle_out(orc, wl):
     return orc.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
 
 
+def appended(pf, wl):
+    """The workload after its append (device tensors, and the numpy workload for the oracle);
+    before it, the slots about to be filled hold NaN."""
+    d = to_device(wl)
+    if wl.slot_mapping is not None:
+        pf.reshape_and_cache(d["new_k"], d["new_v"], d["slot_mapping"], d["k_cache"], d["v_cache"])
+        kc, vc = numpy_scatter(wl)
+        wl = dataclasses.replace(wl, k_cache=kc, v_cache=vc)
+    return d, wl
+
+
 def workspace(fill=None):
     ws = torch.empty(256, dtype=torch.uint8, device="cuda")
     if fill is not None:
@@ -41,8 +54,7 @@ def workspace(fill=None):
 
 @pytest.mark.parametrize("index", [1, 2, 3])
 def test_named_workloads(pf, oracle_lib, config_workload, index):
-    wl = config_workload(index)
-    d = to_device(wl)
+    d, wl = appended(pf, config_workload(index))
     got = persistent(pf, d)
     check_close(got, oracle_out(oracle_lib, wl))
     assert np.array_equal(got, single(pf, d))
@@ -99,7 +111,7 @@ def test_many_short_items_take_the_counter_path(pf, oracle_lib, D, g):
 def test_workspace_contents_do_not_matter(pf, config_workload):
     """Garbage, zeros, and a counter that looks like a finished call: all give the same output,
     and every call leaves the two counters at zero."""
-    d = to_device(config_workload(3))
+    d, _ = appended(pf, config_workload(3))
     ref = single(pf, d)
     rng = np.random.default_rng(5)
     stale = np.zeros(32, dtype=np.uint64)
@@ -129,8 +141,7 @@ def test_workspace_shared_with_the_split(pf, config_workload):
 def test_graph_replays(pf, config_workload):
     """One captured launch replayed with new queries: the counters the previous replay
     cleared serve the next one (the launch's epoch is fixed at capture)."""
-    wl = config_workload(3)
-    d = to_device(wl)
+    d, wl = appended(pf, config_workload(3))
     ws = workspace()
     out = torch.empty((wl.num_seqs, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device="cuda")
     pf.paged_attention_decode_persistent(*attn_args(d), workspace=ws, out=out)  # first call outside capture
@@ -166,7 +177,7 @@ def test_bad_length_and_block_give_nan_rows(pf):
 
 
 def test_deterministic_and_stream_ordered(pf, config_workload):
-    d = to_device(config_workload(3))
+    d, _ = appended(pf, config_workload(3))
     ws = workspace()
     a = persistent(pf, d, ws)
     outs = [pf.paged_attention_decode_persistent(*attn_args(d), workspace=ws) for _ in range(5)]
