@@ -43,7 +43,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 DECODE_SOURCES = ["paged_kv_decode_pf_gb300/csrc/pf_decode.cuh", "paged_kv_decode_pf_gb300/csrc/pf_device.cuh",
-                  "paged_kv_decode_pf_gb300/csrc/pf_internal.h", "paged_kv_decode_pf_gb300/csrc/pf_partition.cuh",
+                  "paged_kv_decode_pf_gb300/csrc/pf_internal.h",
                   "paged_kv_decode_pf_gb300/csrc/pf_decode_d128.cu", "paged_kv_decode_pf_gb300/csrc/pf_decode_d64.cu"]
 
 
@@ -58,8 +58,8 @@ def parse_args():
     ap.add_argument("--oracle-seconds", type=float, default=15.0, help="CPU work of the oracle baseline sample")
     ap.add_argument("--seqs", type=int, default=0,
                     help="profiling aid: keep only the first N sequences of the workload (0 = all)")
-    ap.add_argument("--decode-variant", default="decode", choices=["decode", "persistent", "split"],
-                    help="headline path: single-pass decode (one CTA per item or persistent) or partition+merge")
+    ap.add_argument("--decode-variant", default="decode", choices=["decode", "split"],
+                    help="headline path: single-pass decode or partition+merge")
     return ap.parse_args()
 
 
@@ -83,8 +83,8 @@ def decode_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch of `kernel` recorded by an ncu capture of the current decode sources, if any."""
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch recorded by an ncu capture of the current decode sources, if any."""
     sha = decode_source_sha()
     pat = re.compile(r"traffic-record:\s+workload=(\S+)\s+kernel=(\S+)\s+bytes_per_launch=(\d+)\s+source_sha=(\w+)")
     pdir = os.path.join(ROOT, "profiles")
@@ -95,7 +95,7 @@ def profiled_traffic(workload: str, kernel: str):
             continue
         with open(os.path.join(pdir, name)) as f:
             for m in pat.finditer(f.read()):
-                if m.group(1) == workload and m.group(2) == kernel and m.group(4) == sha:
+                if m.group(1) == workload and m.group(4) == sha:
                     return int(m.group(3))
     return None
 
@@ -190,9 +190,6 @@ class Runner:
             self.max_ctx = wl.max_context_len
             self.ws = pf.alloc_workspace(wl.num_seqs, wl.num_q_heads, wl.head_dim, self.max_ctx, self.P, dev)
         self.fused = self.append and not self.split and variant == "fused"
-        self.persistent = not self.split and not self.fused and variant == "persistent"
-        if self.persistent:
-            self.ws = torch.empty(pf.DECODE_PERSISTENT_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
         self.kernels_per_step = 1 if self.fused else (1 if self.append else 0) + (2 if self.split else 1)
         self.dominant = "partition" if self.split else ("decode_append" if self.fused else "decode")
 
@@ -218,11 +215,6 @@ class Runner:
                 ev[1].record()
             pf.paged_attention_merge(self.ws, self.cl, self.wl.num_q_heads, self.wl.head_dim, self.P, self.max_ctx,
                                      self.out)
-        elif self.persistent:
-            pf.paged_attention_decode_persistent(self.q, self.kc, self.vc, self.bt, self.cl, self.wl.scale, self.ws,
-                                                 self.out)
-            if ev is not None:
-                ev[1].record()
         else:
             pf.paged_attention_decode(self.q, self.kc, self.vc, self.bt, self.cl, self.wl.scale, self.out)
             if ev is not None:
@@ -530,9 +522,8 @@ def main():
             del mr
         del runner
         torch.cuda.empty_cache()
-        for idx, variant in [(1, "decode"), (2, "decode"), (3, "decode"), (3, "fused"), (3, "persistent"),
-                             (4, "decode"), (4, "persistent"), (5, "decode")]:
-            if idx == args.workload and variant == args.decode_variant:
+        for idx, variant in [(1, "decode"), (2, "decode"), (3, "decode"), (3, "fused"), (5, "decode")]:
+            if idx == args.workload and variant == "decode":
                 continue
             w = make_config(idx)
             r = Runner(pf, w, dev, variant)
@@ -542,11 +533,10 @@ def main():
             ms_s, ms_d, _ = time_steps(r, n, 10, fl)
             pf.check_device_error()
             b = r.step_bytes()
-            extras[CONFIGS[idx].name + ("_fused" if r.fused else "_persistent" if r.persistent else "")] = {
+            extras[CONFIGS[idx].name + ("_fused" if r.fused else "")] = {
                 "description": CONFIGS[idx].description,
                 "step": "append and decode fused in one launch" if r.fused else
-                        ("append + " if r.append else "") + ("partition + merge" if r.split else
-                                                             "persistent decode" if r.persistent else "decode"),
+                        ("append + " if r.append else "") + ("partition + merge" if r.split else "decode"),
                 "us_per_step": round(ms_s * 1e3, 2) if fl is None else None,
                 "us_dominant_kernel": round(ms_d * 1e3, 2),
                 "algorithmic_bytes": b,
@@ -604,8 +594,7 @@ def main():
             "us_per_call": round(ms_step * 1e3, 2),
             "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic(CONFIGS[args.workload].name,
-                                                                    runner_kernel(args, wl).split()[0]),
+                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic(CONFIGS[args.workload].name),
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                          else "fallback 6.8 TB/s", "kernel": runner_kernel(args, wl),
                          "kernel_us_mean": round(ms_dom * 1e3, 2),
@@ -658,11 +647,7 @@ def runner_split(args, wl):
 
 
 def runner_kernel(args, wl):
-    if runner_split(args, wl):
-        return "paged_persistent_kernel (partition pass)"
-    if args.decode_variant == "persistent":
-        return "paged_persistent_kernel (single pass)"
-    return "paged_decode_kernel"
+    return "paged_decode_kernel (partition pass)" if runner_split(args, wl) else "paged_decode_kernel"
 
 
 def kernels_per_step(args, wl):

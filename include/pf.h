@@ -139,33 +139,6 @@ PF_API pf_status pf_paged_attention_decode(const void* q, const void* k_cache, c
                                     float scale, float* out, pf_stream_t stream);
 
 /*
- * The same decode attention as pf_paged_attention_decode ("decode-only
- * block-table attention reads physical KV blocks directly", ForgeLLM README,
- * feature list), scheduled differently: a grid of resident CTAs takes the
- * (sequence, kv head) items longest first from a work counter, and each CTA's
- * copy pipeline runs on from one item into the next, so no item pays a CTA's
- * start-up.  Each item's arithmetic is that of pf_paged_attention_decode, so
- * the outputs are identical.  num_seqs <= 512 (PF_ERR_UNSUPPORTED above).
- *
- *   workspace        device memory of at least PF_DECODE_PERSISTENT_WORKSPACE_BYTES,
- *                    256-byte aligned, owned by the caller; it holds the call's work
- *                    counters.  Its contents need no initialisation (a counter left
- *                    by another call, or never written, is recognised and taken
- *                    over) and are left cleared when the call completes.  One
- *                    workspace must not serve two calls that can run at the same
- *                    time (two streams); calls on one stream may share it, and so
- *                    may replays of a captured call.
- * Other arguments, shapes and errors as pf_paged_attention_decode.
- */
-#define PF_DECODE_PERSISTENT_WORKSPACE_BYTES 256u
-PF_API pf_status pf_paged_attention_decode_persistent(const void* q, const void* k_cache, const void* v_cache,
-                                               const int32_t* block_tables, const int32_t* context_lens,
-                                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                                               int block_size, int max_blocks_per_seq, int64_t num_blocks,
-                                               float scale, void* workspace, size_t workspace_bytes,
-                                               float* out, pf_stream_t stream);
-
-/*
  * One decode step in one launch: append each sequence's new token, then attend
  * over the cache that includes it (the write and the read sides of "physical KV
  * blocks with logical per-request block tables" and "decode-only block-table

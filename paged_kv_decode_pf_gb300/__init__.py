@@ -55,9 +55,6 @@ def lib() -> ctypes.CDLL:
         L.pf_reshape_and_cache.restype = st
         L.pf_paged_attention_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, f32, P, P]
         L.pf_paged_attention_decode.restype = st
-        L.pf_paged_attention_decode_persistent.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, f32,
-                                                           P, sz, P, P]
-        L.pf_paged_attention_decode_persistent.restype = st
         L.pf_paged_attention_partition_workspace_layout.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(sz),
                                                                     ctypes.POINTER(sz), ctypes.POINTER(sz)]
         L.pf_paged_attention_partition_workspace_layout.restype = sz
@@ -181,32 +178,6 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                                                block_tables.data_ptr(), context_lens.data_ptr(), S, Hq, Hkv, D, bs,
                                                MB, NB, scale, out.data_ptr(), _stream(q.device)),
                "pf_paged_attention_decode")
-    return out
-
-
-DECODE_PERSISTENT_WORKSPACE_BYTES = 256  # PF_DECODE_PERSISTENT_WORKSPACE_BYTES
-
-
-def paged_attention_decode_persistent(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
-                                      block_tables: torch.Tensor, context_lens: torch.Tensor,
-                                      scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
-                                      out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Single-pass decode attention on resident CTAs that take the (sequence, kv head) items longest
-    first from a work counter in `workspace` (>= 256 bytes, any contents; one per concurrent stream).
-    Returns out [S, Hq, D] fp32, identical to paged_attention_decode's."""
-    S, Hq, Hkv, D, bs, NB, MB = _attn_shapes(q, k_cache, v_cache, block_tables, context_lens)
-    if workspace is None:
-        workspace = torch.empty(DECODE_PERSISTENT_WORKSPACE_BYTES, dtype=torch.uint8, device=q.device)
-    _cuda(workspace, "workspace", (torch.uint8,), 1)
-    if out is None:
-        out = torch.empty((S, Hq, D), dtype=torch.float32, device=q.device)
-    _cuda(out, "out", (torch.float32,), 3)
-    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
-    with torch.cuda.device(q.device):
-        _check(lib().pf_paged_attention_decode_persistent(
-            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
-            S, Hq, Hkv, D, bs, MB, NB, scale, workspace.data_ptr(), workspace.numel(), out.data_ptr(),
-            _stream(q.device)), "pf_paged_attention_decode_persistent")
     return out
 
 

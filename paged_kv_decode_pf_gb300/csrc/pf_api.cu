@@ -270,15 +270,6 @@ static int log2_int(int x) {
 
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Epoch of a persistent single-pass call: tags its work counters; never 0, the value
-// the counters are left at.
-static std::atomic<unsigned> g_epoch{0};
-static unsigned next_epoch() {
-    unsigned e = g_epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
-    while (e == 0u) e = g_epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
-    return e;
-}
-
 // a * b * c * d without overflow of size_t, or SIZE_MAX
 static size_t mul_sat(size_t a, size_t b) { return (b != 0 && a > SIZE_MAX / b) ? SIZE_MAX : a * b; }
 
@@ -403,32 +394,6 @@ pf_status pf_paged_attention_decode(const void* q, const void* k_cache, const vo
     p.out = out;
     p.order_mode = (num_seqs > 1 && num_seqs <= kMaxSortedSeqsDecode) ? ORDER_SORTED : ORDER_NATURAL;
     const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, MODE_DECODE,
-                                        reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
-}
-
-pf_status pf_paged_attention_decode_persistent(const void* q, const void* k_cache, const void* v_cache,
-                                               const int32_t* block_tables, const int32_t* context_lens,
-                                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                                               int block_size, int max_blocks_per_seq, int64_t num_blocks,
-                                               float scale, void* workspace, size_t workspace_bytes, float* out,
-                                               pf_stream_t stream) {
-    const AttnArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
-                     head_dim, block_size, max_blocks_per_seq, num_blocks, scale};
-    pf_status st = check_attention(a);
-    if (st != PF_OK) return st;
-    if (num_seqs > kMaxSortedSeqsDecode) return PF_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return PF_OK;
-    if (!aligned(out, 16) || !aligned(workspace, 256) || workspace_bytes < PF_DECODE_PERSISTENT_WORKSPACE_BYTES)
-        return PF_ERR_INVALID_ARG;
-    unsigned* err = nullptr;
-    if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
-    DecodeParams p = make_params(a, err);
-    p.out = out;
-    p.order_mode = ORDER_SORTED;
-    p.work_counters = static_cast<unsigned long long*>(workspace);
-    p.epoch = next_epoch();
-    const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, MODE_DECODE_PERSISTENT,
                                         reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }

@@ -41,17 +41,12 @@ struct DecodeParams {
     const int64_t* slot_mapping;  // [S]
     uint16_t* k_cache_w;
     uint16_t* v_cache_w;
-    // persistent single pass only: two 64-bit work counters in the caller's workspace
-    // (next item, CTAs finished), each tagged with the call's epoch in its high half
-    unsigned long long* work_counters;
-    unsigned epoch;
 };
 
 // What one launch of the decode kernel computes.
 constexpr int MODE_DECODE = 0;          // single pass over each whole sequence
 constexpr int MODE_PARTITION = 1;       // one context partition per CTA, partials to the workspace
 constexpr int MODE_DECODE_APPEND = 2;   // single pass, after writing each sequence's new token
-constexpr int MODE_DECODE_PERSISTENT = 3;  // single pass, resident CTAs fetch items longest first
 
 // How CTAs map to work items.
 //  ORDER_NATURAL: CTA b serves (sequence b / Hkv, kv head b % Hkv); partition pass:

@@ -1,39 +1,22 @@
-// Persistent kernels: the partition pass of the split over context partitions,
-// and a single pass whose resident CTAs take (sequence, kv head) items longest
-// first from a work counter.
+// Persistent partition pass of the split over context partitions.
 //
 // The partition pass has many short work units -- (sequence, partition, kv head),
 // e.g. 2,072 units of 512 tokens for one 131072-token sequence and three short
 // ones -- and a kernel with one CTA per unit pays each CTA's start-up (lengths,
 // table entries, first tiles: a few microseconds) over and over.  Here a grid of
-// resident CTAs walks the units, and each warp's copy ring runs on across unit
-// boundaries: lane 0 keeps a look-ahead cursor over the warp's future (unit, tile)
-// positions and a small FIFO of their table entries, so the next unit's tiles are
-// already in flight while the current one finishes.  Each unit ends with the CTA
-// merging its warps' (m, l, acc) in a dedicated shared-memory area and writing the
-// partial (partition pass) or the output rows (single pass).
-//
-// Which units a CTA takes:
-//  partition pass: round-robin, CTA c takes units c, c + grid, ... of the flattened
-//    non-empty (sequence, partition) pairs -- the units are equal but for the last
-//    partition of each sequence, so a static assignment balances;
-//  single pass: the units are whole (sequence, kv head) items of any length, ranked
-//    longest first (every CTA ranks the lengths in shared memory).  CTA c starts with
-//    ranks c and c + grid; every later unit is the next value of a counter in the
-//    caller's workspace (thread 0 asks for unit j + 2 when unit j starts and publishes
-//    the answer when it ends), so CTAs that drew short items take more of them --
-//    longest-processing-time-first list scheduling without a CTA start-up per item.
-//    The counter and a count of finished CTAs carry the call's epoch in their high
-//    32 bits: a value from another call (or never-written memory) is taken over, and
-//    the last CTA to finish sets both back to zero, so a replay of the same launch
-//    (a CUDA graph) starts clean.  One workspace must not serve two calls at once.
+// resident CTAs walks the units round-robin (CTA c takes units c, c + grid, ...),
+// and each warp's copy ring runs on across unit boundaries: lane 0 keeps a
+// look-ahead cursor over the warp's future (unit, tile) positions and a small
+// FIFO of their table entries, so the next unit's tiles are already in flight
+// while the current one finishes.  Each unit ends with the CTA merging its warps'
+// (m, l, acc) in a dedicated shared-memory area and writing the partial.
 #pragma once
 
 #include "pf_decode.cuh"
 
 namespace pf {
 
-template <int D, int G, int NW, int NST, bool DEC>
+template <int D, int G, int NW, int NST>
 struct PersistentLayout {
     using Geo = DecodeGeometry<D, G>;
     static constexpr size_t STAGES = size_t(NW) * NST * 2 * Geo::TILE_BYTES;
@@ -42,65 +25,10 @@ struct PersistentLayout {
     static constexpr size_t MML = MACC + size_t(NW) * G * D * 4;                    // [NW][2G]
     static constexpr size_t BAD = MML + (size_t(NW) * 2 * G * 4 + 15) / 16 * 16;    // [NW][NST] stage flags
     static constexpr size_t BARS = BAD + (size_t(NW) * NST * 4 + 15) / 16 * 16;     // [NW][NST] mbarriers
-    static constexpr size_t KEYS = BARS + (size_t(NW) * NST * 8 + 15) / 16 * 16;    // round_up(S,4) ints
-    // partition pass: the prefix of partition counts; single pass: ranking keys, then
-    // the order (sequence of each rank), round_up(S,4) ints each
-    static size_t bytes(int num_seqs) { return KEYS + size_t((num_seqs + 3) & ~3) * 4 * (DEC ? 2 : 1); }
-    static constexpr size_t max_bytes() {
-        return KEYS + size_t(DEC ? 2 * kMaxSortedSeqsDecode : kMaxSortedSeqsPartition) * 4;
-    }
+    static constexpr size_t KEYS = BARS + (size_t(NW) * NST * 8 + 15) / 16 * 16;    // prefix, round_up(S,4)
+    static size_t bytes(int num_seqs) { return KEYS + size_t((num_seqs + 3) & ~3) * 4; }
+    static constexpr size_t max_bytes() { return KEYS + size_t(kMaxSortedSeqsPartition) * 4; }
 };
-
-// Longest-first order of the sequences: order[r] = the sequence of rank r, by length
-// with ties broken by index (the order of the sorted one-CTA-per-item decode).
-// keys: round_up(S,4) ints of scratch.  S <= 1024.
-template <int NW>
-__device__ __forceinline__ void lpt_order(const DecodeParams& p, int* keys, int* order) {
-    constexpr int NT = NW * 32;
-    const int S = p.num_seqs;
-    const int Sp = (S + 3) & ~3;
-    for (int i = threadIdx.x; i < Sp; i += NT) {
-        int key = -1;
-        if (i < S) {
-            const int Li = min(max(__ldg(p.context_lens + i), 0), (1 << 20) - 1);
-            key = (Li << 10) | (1023 - i);
-        }
-        keys[i] = key;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < S; i += NT) {
-        const int ki = keys[i];
-        int rank = 0;
-        for (int j = 0; j < Sp; j += 4) {
-            const int4 kj = *reinterpret_cast<const int4*>(keys + j);
-            rank += int(kj.x > ki) + int(kj.y > ki) + int(kj.z > ki) + int(kj.w > ki);
-        }
-        order[rank] = i;
-    }
-    __syncthreads();
-}
-
-// Resolve the value old = atomicAdd(c, 1) returned on a counter tagged with the call's
-// epoch (high 32 bits) into this call's count.  A counter still holding another epoch
-// is taken over by installing (epoch, 1), which gives count 0 to the installer; the
-// others count again under the new epoch.  0xffffffff if it could not settle.
-static __device__ __noinline__ unsigned tagged_count(unsigned long long* c, unsigned epoch, unsigned long long old) {
-    if (unsigned(old >> 32) == epoch) return unsigned(old);
-    const unsigned long long mine = (static_cast<unsigned long long>(epoch) << 32) | 1ull;
-    unsigned long long expect = old + 1ull;
-    for (int it = 0; it < 4096; ++it) {
-        const unsigned long long seen = atomicCAS(c, expect, mine);
-        if (seen == expect) return 0u;
-        if (unsigned(seen >> 32) == epoch) {
-            const unsigned long long again = atomicAdd(c, 1ull);
-            if (unsigned(again >> 32) == epoch) return unsigned(again);
-            expect = again + 1ull;
-        } else {
-            expect = seen;
-        }
-    }
-    return 0xffffffffu;
-}
 
 // Inclusive prefix over sequences of their non-empty partition counts, into
 // keys[0..S); lengths outside [0, max_context_len] count as 0 (the merge NaN-fills
@@ -175,28 +103,10 @@ __device__ __forceinline__ PartUnit decode_unit(const DecodeParams& p, const int
     return x;
 }
 
-// A single-pass unit: rank u / Hkv of the longest-first order, kv head u % Hkv.
-template <int NW>
-__device__ __forceinline__ PartUnit decode_item(const DecodeParams& p, const int* order, int u, int warp) {
-    PartUnit x;
-    const int rank = u / p.num_kv_heads;
-    x.kvh = u - rank * p.num_kv_heads;
-    x.seq = order[rank];
-    x.part = 0;
-    const int L = __ldg(p.context_lens + x.seq);
-    x.bad = L < 0 || (long long)L > (long long)p.max_blocks_per_seq * p.block_size;
-    x.t0 = 0;
-    x.t1 = x.bad ? 0 : L;
-    const int ntiles = (x.t1 + kTileTokens - 1) / kTileTokens;
-    x.nkw = ntiles > warp ? (ntiles - warp + NW - 1) / NW : 0;
-    x.trow = p.block_tables + size_t(x.seq) * p.max_blocks_per_seq;
-    return x;
-}
-
-template <int D, int G, int NW, int NST, bool DEC>
-__global__ void __launch_bounds__(NW * 32, 3) paged_persistent_kernel(const DecodeParams p) {
+template <int D, int G, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32) paged_partition_persistent_kernel(const DecodeParams p) {
     using Geo = DecodeGeometry<D, G>;
-    using Lay = PersistentLayout<D, G, NW, NST, DEC>;
+    using Lay = PersistentLayout<D, G, NW, NST>;
     constexpr int TT = Geo::TT, ROW = Geo::ROW_BYTES, TILE = Geo::TILE_BYTES, PSM_PAD = Geo::PSM_PAD;
     constexpr int R = NST + 2;  // look-ahead depth of lane 0's table FIFO
 
@@ -207,54 +117,14 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_persistent_kernel(const Deco
     int* stage_bad = reinterpret_cast<int*>(smem + Lay::BAD);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::BARS);
     int* keys = reinterpret_cast<int*>(smem + Lay::KEYS);
-    int* order = keys + ((p.num_seqs + 3) & ~3);  // single pass only
-    __shared__ volatile int s_tick[4];  // single pass: unit of CTA-local index j at [j % 4], for j <= s_pub
-    __shared__ volatile int s_pub;
-    __shared__ int unit_failed[NW];
 
     // The merge that follows may be scheduled as SMs drain; it waits for this grid to complete.
-    if constexpr (!DEC) asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.launch_dependents;");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
-    if (threadIdx.x == 0) s_pub = 1;  // units 0 and 1 of a CTA are fixed
-    int U;
-    if constexpr (DEC) {
-        lpt_order<NW>(p, keys, order);
-        U = p.num_seqs * Hkv;
-    } else {
-        U = partition_prefix<NW>(p, keys) * Hkv;
-    }
-    // single pass: count this CTA as finished; the last one clears the counters
-    auto finish = [&]() {
-        if constexpr (DEC) {
-            if (threadIdx.x == 0) {
-                __threadfence();
-                const unsigned long long old = atomicAdd(p.work_counters + 1, 1ull);
-                const unsigned n = tagged_count(p.work_counters + 1, p.epoch, old);
-                if (n == gridDim.x - 1) {
-                    atomicExch(p.work_counters, 0ull);
-                    atomicExch(p.work_counters + 1, 0ull);
-                } else if (n == 0xffffffffu) {
-                    set_error(p.err, ERR_TIMEOUT);
-                }
-            }
-        }
-    };
-    if (int(blockIdx.x) >= U) {
-        finish();
-        return;
-    }
-    auto unit_of = [&](int j) -> int {  // CTA-local unit j; -1 while it is not known yet
-        if constexpr (DEC) {
-            if (j >= 2) return j <= s_pub ? s_tick[j & 3] : -1;
-        }
-        return int(blockIdx.x) + j * int(gridDim.x);
-    };
-    auto unit_at = [&](int u) {
-        if constexpr (DEC) return decode_item<NW>(p, order, u, warp);
-        else return decode_unit<NW>(p, keys, u, warp);
-    };
+    const int U = partition_prefix<NW>(p, keys) * Hkv;
+    if (int(blockIdx.x) >= U) return;
 
     unsigned char* my_stages = smem + size_t(warp) * NST * 2 * TILE;
     const uint32_t stage0 = smem_u32(my_stages);
@@ -273,55 +143,33 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_persistent_kernel(const Deco
     auto block_offset = [&](int tok) { return bshift >= 0 ? (tok & (bs - 1)) : (tok % bs); };
     const uint64_t policy = l2_policy_evict_first();
 
-    // ---- lane 0: look-ahead cursor over (unit, tile) and a FIFO of the next R positions.
-    // FIFO slot state f_n: > 0 rows of a known position, 0 past the last unit, -1 not
-    // known yet (the cursor waits for a unit's publication; such slots form a suffix).
+    // ---- lane 0: look-ahead cursor over (unit, tile) and a FIFO of the next R positions
     int look_j = 0, look_i = 0;
     PartUnit look{};
-    bool look_done = false, look_blocked = false;
-    auto look_unit = [&]() {  // settle on the first unit from look_j on where this warp has tiles
-        look_blocked = false;
+    bool look_done = false;
+    auto look_unit = [&]() {  // settle on the first unit (from look_j on) where this warp has tiles
         for (;;) {
-            const int u = unit_of(look_j);
-            if (u < 0) { look_blocked = true; return; }
+            const int u = int(blockIdx.x) + look_j * int(gridDim.x);
             if (u >= U) { look_done = true; return; }
-            look = unit_at(u);
+            look = decode_unit<NW>(p, keys, u, warp);
             if (look.nkw > 0) { look_i = 0; return; }
             ++look_j;
         }
     };
-    int f_pb[R], f_row[R], f_n[R];  // table entry, first cache row of the tile (kvh, offset), rows
-    auto take = [&](int& pb, int& row, int& nrows) {  // the cursor's position; advance the cursor
+    int f_pb[R], f_row[R], f_n[R];  // FIFO: table entry, first cache row of the tile (kvh, offset), rows
+    auto push_back = [&](int slot) {
+        if (look_done) { f_n[slot] = 0; return; }
         const int tok = look.t0 + (warp + NW * look_i) * TT;
-        pb = __ldg(look.trow + block_index(tok));
-        row = look.kvh * bs + block_offset(tok);  // + pb * Hkv * bs once the entry is in
-        nrows = min(TT, look.t1 - tok);
+        f_pb[slot] = __ldg(look.trow + block_index(tok));
+        f_row[slot] = look.kvh * bs + block_offset(tok);  // + pb * Hkv * bs once the entry is in
+        f_n[slot] = min(TT, look.t1 - tok);
         if (++look_i >= look.nkw) { ++look_j; look_unit(); }
     };
-    auto resolve = [&]() {  // fill the not-yet-known suffix as far as the cursor can go now
-        if (!look_blocked) return;
-        look_unit();
-#pragma unroll
-        for (int k = 0; k < R; ++k) {
-            if (f_n[k] == -1 && !look_blocked) {
-                if (look_done) f_n[k] = 0;
-                else take(f_pb[k], f_row[k], f_n[k]);
-            }
-        }
-    };
-    auto push_back = [&]() {  // slot R - 1, after a shift
-        resolve();
-        if (look_done) f_n[R - 1] = 0;
-        else if (look_blocked) f_n[R - 1] = -1;
-        else take(f_pb[R - 1], f_row[R - 1], f_n[R - 1]);
-    };
     int n_issued = 0;
-    auto issue_front = [&]() -> bool {  // copy the FIFO's front into the next stage; false: not known yet
-        resolve();
-        if (f_n[0] < 0) return false;
+    auto issue_front = [&]() {  // copy the FIFO's front position into the next stage, refill the FIFO
+        const int s = n_issued % NST;
+        const uint32_t bar = bar0 + 8 * s;
         if (f_n[0] > 0) {
-            const int s = n_issued % NST;
-            const uint32_t bar = bar0 + 8 * s;
             const int pb = f_pb[0];
             if (pb >= 0 && (long long)pb < p.num_blocks) {
                 const uint32_t bytes = uint32_t(f_n[0]) * ROW;
@@ -332,7 +180,7 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_persistent_kernel(const Deco
                 bulk_copy_g2s(dst, p.k_cache + row * D, bytes, bar, policy);
                 bulk_copy_g2s(dst + TILE, p.v_cache + row * D, bytes, bar, policy);
             } else {
-                my_bad[s] = 1;  // no copy: the unit's result ends up NaN
+                my_bad[s] = 1;  // no copy: the unit's partial ends up NaN
                 set_error(p.err, ERR_BOUNDS);
                 mbar_arrive(bar);
             }
@@ -344,40 +192,27 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_persistent_kernel(const Deco
             f_row[k] = f_row[k + 1];
             f_n[k] = f_n[k + 1];
         }
-        push_back();
-        return true;
-    };
-    auto pump = [&](int n_consumed) {  // keep NST positions in flight where they are known
-        while (n_issued < n_consumed + NST && f_n[0] != 0) {
-            if (!issue_front()) break;
-        }
+        push_back(R - 1);
     };
     if (lane == 0) {
         look_unit();
 #pragma unroll
-        for (int k = 0; k < R; ++k) {
-            if (look_done) f_n[k] = 0;
-            else if (look_blocked) f_n[k] = -1;
-            else take(f_pb[k], f_row[k], f_n[k]);
-        }
-        pump(0);
+        for (int k = 0; k < R; ++k) push_back(k);
+#pragma unroll
+        for (int k = 0; k < NST; ++k) issue_front();
     }
 
     // ---- consumer: the same positions, unit by unit
     WarpAttention<D, G> wa;
     wa.init(lane);
+    __shared__ int unit_failed[NW];
     int n = 0;             // positions consumed: stage n % NST, phase (n / NST) & 1
     bool dead = false;     // a wait gave up: consume nothing more, keep the CTA's barriers
-    bool more = true;      // thread 0, single pass: the counter may still hold units
     int q_seq = -1, q_kvh = -1;
     for (int j = 0;; ++j) {
-        const int u = unit_of(j);
-        if (u < 0 || u >= U) break;
-        const PartUnit x = unit_at(u);
-        // single pass: ask for unit j + 2 now, use the answer when unit j ends
-        unsigned long long asked = 0;
-        const bool ask = DEC && threadIdx.x == 0 && more;
-        if (ask) asked = atomicAdd(p.work_counters, 1ull);
+        const int u = int(blockIdx.x) + j * int(gridDim.x);
+        if (u >= U) break;
+        const PartUnit x = decode_unit<NW>(p, keys, u, warp);
         if (x.seq != q_seq || x.kvh != q_kvh) {
             wa.load_q(p.q + (size_t(x.seq) * Hq + x.kvh * G) * D);
             q_seq = x.seq;
@@ -386,11 +221,8 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_persistent_kernel(const Deco
         wa.reset();
         bool failed = x.bad || dead;
         for (int i = 0; i < x.nkw && !dead; ++i) {
-            if (lane == 0) pump(n);
             const int s = n % NST;
-            // position n is always issued by now (its unit is known); checked rather than assumed
-            bool ok = __shfl_sync(FULL_MASK, n < n_issued ? 1 : 0, 0) != 0;
-            if (ok) ok = mbar_wait_bounded(bar0 + 8 * s, (n / NST) & 1, p.wait_limit_ns);
+            const bool ok = mbar_wait_bounded(bar0 + 8 * s, (n / NST) & 1, p.wait_limit_ns);
             if (__any_sync(FULL_MASK, !ok)) {
                 dead = true;
                 failed = true;
@@ -402,7 +234,7 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_persistent_kernel(const Deco
             const int tok = x.t0 + (warp + NW * i) * TT;
             wa.tile(Ks, Ks + TILE, min(TT, x.t1 - tok), psm, p.scale_log2);
             ++n;
-            if (lane == 0) pump(n);
+            if (lane == 0) issue_front();
         }
         wa.stash(mml + warp * 2 * G, macc + warp * G * D);
         if (lane == 0) unit_failed[warp] = failed ? 1 : 0;
@@ -411,49 +243,28 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_persistent_kernel(const Deco
 #pragma unroll
         for (int w = 0; w < NW; ++w) any_failed = any_failed || unit_failed[w] != 0;
         if (x.bad && threadIdx.x == 0) set_error(p.err, ERR_BOUNDS);
-        if constexpr (DEC) {
-            merge_warps_and_store<D, G, NW>([&](int w) { return mml + w * 2 * G; },
-                                            [&](int w) { return (const float*)(macc + w * G * D); }, any_failed,
-                                            p.out + (size_t(x.seq) * Hq + x.kvh * G) * D, nullptr, nullptr, 1);
-            if (threadIdx.x == 0) {
-                int t = U;
-                if (ask) {
-                    const unsigned c = tagged_count(p.work_counters, p.epoch, asked);
-                    if (c == 0xffffffffu) set_error(p.err, ERR_TIMEOUT);
-                    else t = int(min(2ll * gridDim.x + (long long)c, (long long)U));
-                }
-                if (t >= U) more = false;
-                s_tick[(j + 2) & 3] = t;
-                s_pub = j + 2;
-            }
-        } else {
-            const size_t slot0 = (size_t(x.seq) * Hq + x.kvh * G) * p.num_partitions + x.part;
-            merge_warps_and_store<D, G, NW>([&](int w) { return mml + w * 2 * G; },
-                                            [&](int w) { return (const float*)(macc + w * G * D); }, any_failed,
-                                            p.out + slot0 * D, p.part_m + slot0, p.part_l + slot0,
-                                            size_t(p.num_partitions));
-        }
+        const size_t slot0 = (size_t(x.seq) * Hq + x.kvh * G) * p.num_partitions + x.part;
+        merge_warps_and_store<D, G, NW>([&](int w) { return mml + w * 2 * G; },
+                                        [&](int w) { return (const float*)(macc + w * G * D); }, any_failed,
+                                        p.out + slot0 * D, p.part_m + slot0, p.part_l + slot0,
+                                        size_t(p.num_partitions));
         __syncthreads();
-        if constexpr (DEC) {
-            if (lane == 0 && !dead) pump(n);  // the published unit may let the cursor move on
-        }
     }
     if (lane == 0) {
         // no copy may still be landing when the CTA exits (only after a wait gave up)
         for (int k = n; k < n_issued; ++k) mbar_wait_bounded(bar0 + 8 * (k % NST), (k / NST) & 1, p.wait_limit_ns);
     }
     __syncwarp();
-    finish();
 }
 
 }  // namespace pf
 
 namespace pf {
 
-template <int D, int G, int NW, int NST, bool DEC>
-cudaError_t launch_persistent(const DecodeParams& p, cudaStream_t stream) {
-    using Lay = PersistentLayout<D, G, NW, NST, DEC>;
-    auto kern = paged_persistent_kernel<D, G, NW, NST, DEC>;
+template <int D, int G, int NW, int NST>
+cudaError_t launch_partition_persistent(const DecodeParams& p, cudaStream_t stream) {
+    using Lay = PersistentLayout<D, G, NW, NST>;
+    auto kern = paged_partition_persistent_kernel<D, G, NW, NST>;
     static std::atomic<unsigned long long> configured{0};  // one bit per device ordinal
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -470,8 +281,7 @@ cudaError_t launch_persistent(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     e = sm_count(&sms);
     if (e != cudaSuccess) return e;
-    // the partition pass has at most this many units; the single pass exactly S * Hkv
-    const long long upper = (long long)(DEC ? 1 : p.num_partitions) * p.num_kv_heads * p.num_seqs;
+    const long long upper = (long long)p.num_partitions * p.num_kv_heads * p.num_seqs;  // units can't exceed it
     long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
     if (grid > upper) grid = upper;
     if (grid <= 0) return cudaSuccess;
@@ -485,10 +295,9 @@ cudaError_t launch_decode_mode(const DecodeParams& p, int mode, cudaStream_t str
         case MODE_DECODE: return launch_decode_variant<D, G, NW, NST, MODE_DECODE>(p, stream);
         case MODE_PARTITION:
             // the persistent pass needs the flattened (sorted) unit order
-            return p.order_mode == ORDER_SORTED ? launch_persistent<D, G, NW, NST, false>(p, stream)
+            return p.order_mode == ORDER_SORTED ? launch_partition_persistent<D, G, NW, NST>(p, stream)
                                                 : launch_decode_variant<D, G, NW, NST, MODE_PARTITION>(p, stream);
         case MODE_DECODE_APPEND: return launch_decode_variant<D, G, NW, NST, MODE_DECODE_APPEND>(p, stream);
-        case MODE_DECODE_PERSISTENT: return launch_persistent<D, G, NW, NST, true>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

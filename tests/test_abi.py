@@ -102,22 +102,6 @@ def test_partition_and_merge_host_validation(lib):
     assert m(None, None, 0, 8, 128, 32, 64, None, None) == 0
 
 
-def test_persistent_decode_host_validation(lib):
-    P = ctypes.c_void_p
-    f = lib.pf_paged_attention_decode_persistent
-
-    def call(S=2, ws=0x70000, ws_bytes=256, out=0x60000):
-        return f(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, S, 8, 2, 128, 16, 4, 64, ctypes.c_float(0.1),
-                 P(ws), ws_bytes, P(out), None)
-    assert call(S=513) == 2                                          # above the ranking limit
-    assert call(ws_bytes=255) == 1                                   # workspace too small
-    assert call(ws=0x70010) == 1                                     # workspace misaligned
-    assert call(ws=0) == 1                                           # no workspace
-    assert call(out=0x60004) == 1
-    assert f(None, None, None, None, None, 0, 8, 2, 128, 16, 4, 64, ctypes.c_float(0.1), None, 0, None,
-             None) == 0                                              # no sequences: nothing to do
-
-
 def test_append_host_validation(lib):
     f = lib.pf_reshape_and_cache
     ok = [0x10000, 0x20000, 0x30000, 0x40000, 0x50000]
