@@ -331,6 +331,13 @@ class MultiQueryRunner:
         rows = wl.num_seqs * self.q_len * wl.num_q_heads * wl.head_dim
         return wl.algorithmic_bytes() - wl.num_seqs * wl.num_q_heads * wl.head_dim * 6 + rows * 6
 
+    def step_flops(self):
+        """Useful flops: 4 D per (query row, visible token) -- Q.K and P.V, causal limits applied."""
+        wl = self.r.wl
+        L = wl.context_lens.astype(np.int64)
+        vis = sum(np.clip(L - self.q_len + j + 1, 0, None).sum() for j in range(self.q_len))
+        return int(4 * wl.head_dim * wl.num_q_heads * vis)
+
 
 class CopyRunner:
     """pf_copy_blocks over `pairs` random (src, dst) pairs of Llama-3-8B-shaped blocks
@@ -505,18 +512,23 @@ def main():
 
     extras = {}
     if not args.no_extras and rank == 0:
-        if not runner.split and wl.num_q_heads // wl.num_kv_heads * 4 <= 16:
-            # the same resident cache, with the last 4 tokens of every sequence as new (draft) tokens
-            mr = MultiQueryRunner(pf, runner, 4)
+        g = wl.num_q_heads // wl.num_kv_heads
+        for q_len in (4, 8, 16):
+            if runner.split or g * q_len > 64:
+                continue
+            # the same resident cache, with the last q_len tokens of every sequence as new (draft) tokens
+            mr = MultiQueryRunner(pf, runner, q_len)
             ms_s, ms_d, _ = time_steps(mr, 200, 10)
             pf.check_device_error()
             mb = mr.step_bytes()
-            extras[CONFIGS[args.workload].name + "_multi_query_q4"] = {
-                "description": "pf_paged_attention_multi_query on the same cache: 4 new tokens per sequence, "
-                               "causal among them",
+            fl = mr.step_flops()
+            extras[CONFIGS[args.workload].name + f"_multi_query_q{q_len}"] = {
+                "description": f"pf_paged_attention_multi_query on the same cache: {q_len} new tokens per "
+                               f"sequence, causal among them ({g * q_len} query rows per kv head)",
                 "step": "multi_query", "us_dominant_kernel": round(ms_d * 1e3, 2), "algorithmic_bytes": mb,
                 "gbs_dominant_kernel": round(mb / (ms_d * 1e-3) / 1e9, 1),
                 "pct_of_8tbs_dominant": round(100 * mb / (ms_d * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
+                "tflops_dominant_kernel": round(fl / (ms_d * 1e-3) / 1e12, 1),
                 "l2": "inputs larger than L2",
             }
             del mr

@@ -178,12 +178,15 @@ PF_API pf_status pf_paged_attention_decode_append(const void* q, const void* k_n
  *
  * A row whose position is negative (L_i < q_len) is zero.  The scores and P.V
  * run on tensor cores (mma.sync, bf16 inputs, fp32 accumulation; the
- * probabilities enter P.V as a bf16 high part plus a bf16 remainder).
+ * probabilities enter P.V as a bf16 high part plus a bf16 remainder).  Up to 16
+ * rows per kv head (g * q_len) one CTA's four warps split the tokens; from 17 to
+ * 64 rows each 16-row tile has its own warp and a producer warp streams K/V to
+ * all of them.
  *
  *   q    [num_seqs, q_len, num_q_heads, head_dim] bf16, 16-byte aligned
  *   out  [num_seqs, q_len, num_q_heads, head_dim] fp32
  * Supported: head_dim in {64, 128}, block_size a multiple of 16,
- * (num_q_heads / num_kv_heads) * q_len <= 16, num_blocks * num_kv_heads *
+ * (num_q_heads / num_kv_heads) * q_len <= 64, num_blocks * num_kv_heads *
  * block_size < 2^31; other arguments and errors as pf_paged_attention_decode.
  */
 PF_API pf_status pf_paged_attention_multi_query(const void* q, const void* k_cache, const void* v_cache,

@@ -209,7 +209,7 @@ def paged_attention_multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
                                 block_tables: torch.Tensor, context_lens: torch.Tensor,
                                 scale: Optional[float] = None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """q [S, q_len, Hq, D]: the last q_len tokens of each sequence, already in the cache, attend causally.
-    Returns out [S, q_len, Hq, D] fp32.  Needs (Hq / Hkv) * q_len <= 16."""
+    Returns out [S, q_len, Hq, D] fp32.  Needs (Hq / Hkv) * q_len <= 64."""
     _cuda(q, "q", _BF16, 4)
     _cuda(k_cache, "k_cache", _BF16, 4)
     _cuda(v_cache, "v_cache", _BF16, 4)

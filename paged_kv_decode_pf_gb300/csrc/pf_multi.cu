@@ -22,6 +22,8 @@
 //    against the same V fragments, ldmatrix.trans) so the probabilities keep
 //    about 16 significant bits.
 //  * The 4 warps merge (m, l, O) in shared memory at the end.
+// Above 16 rows (up to 64) a second kernel gives each 16-row tile its own warp and
+// shares the K/V stages among them (below).
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -336,6 +338,295 @@ __global__ void __launch_bounds__(NW * 32) paged_multi_query_kernel(const __grid
     }
 }
 
+// ---------------------------------------------------------------- wide variant
+//
+// More than 16 query rows per kv head (g * q_len up to 64: e.g. 16 draft tokens at
+// g = 4, or a 64-token prompt chunk of a multi-head model).  One CTA per
+// (sequence, kv head) with MT consumer warps, warp w owning query rows
+// [16w, 16w + 16) as one m16 tile, and one producer warp.  The producer's lane 0
+// streams the sequence in stages of 64 tokens (four 16-token tiles, K and V, by TMA
+// tensor copies with the 128-byte swizzle) through an NST-deep ring shared by all
+// consumers: a "full" mbarrier per stage completes when its bytes land, an "empty"
+// one when every consumer has read it.  Each consumer runs the same per-tile
+// arithmetic as the 16-row kernel on its rows and writes them itself.
+constexpr int kWideMaxRows = 64;
+constexpr int kWideSub = 4;     // 16-token tiles per stage
+constexpr int kWideStages = 3;
+
+template <int D, int NST>
+struct WideLayout {
+    static constexpr int TT = kTileTokens;
+    static constexpr int HALVES = D / 64;
+    static constexpr int HALF_BYTES = TT * 128;             // one TMA box: 16 rows x 128 B
+    static constexpr int SUBTILE = HALVES * HALF_BYTES;     // one 16-token tile of K or V
+    static constexpr int KV = kWideSub * SUBTILE;           // the K (or V) part of a stage
+    static constexpr int STAGE = 2 * KV;
+    static constexpr size_t FULL = size_t(NST) * STAGE;     // NST mbarriers
+    static constexpr size_t EMPTY = FULL + size_t(NST) * 8;  // NST mbarriers
+    static constexpr size_t BAD = EMPTY + size_t(NST) * 8;   // NST ints: bit u = tile u had no copy
+    static constexpr size_t BYTES = BAD + ((NST * 4 + 15) / 16) * 16;
+    static constexpr size_t ALLOC = BYTES + 1024;           // room to align to 1024
+};
+
+template <int D, int MT, int NST>
+__global__ void __launch_bounds__((MT + 1) * 32) paged_multi_query_wide_kernel(
+    const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v, const MultiParams p) {
+    using Lay = WideLayout<D, NST>;
+    constexpr int TT = Lay::TT, HALVES = Lay::HALVES, HALF = Lay::HALF_BYTES, SUBTILE = Lay::SUBTILE;
+    constexpr int KV = Lay::KV, STAGE = Lay::STAGE;
+    constexpr int SUBTOK = kWideSub * TT;  // tokens per stage
+    constexpr int KSTEPS = D / 16;         // k-steps of S = Q K^T
+    constexpr int NTD = D / 8;             // n-tiles of O = P V
+
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // swizzled boxes need 1 KiB alignment
+    const uint32_t full0 = smem_u32(smem + Lay::FULL), empty0 = smem_u32(smem + Lay::EMPTY);
+    volatile int* bad = reinterpret_cast<volatile int*>(smem + Lay::BAD);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Hkv = p.num_kv_heads, G = p.group, Q = p.q_len, RR = p.rows, Hq = p.num_q_heads;
+    const int seq = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
+    const int L = __ldg(p.context_lens + seq);
+    const bool len_bad = L < 0 || (long long)L > (long long)p.max_blocks_per_seq * p.block_size;
+    auto out_row = [&](int r) -> float* {  // query row r = j * G + h
+        const int j = r / G, h = r - (r / G) * G;
+        return p.out + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D;
+    };
+    if (len_bad) {
+        if (threadIdx.x == 0) set_error(p.err, ERR_BOUNDS);
+        for (int e = threadIdx.x; e < RR * D; e += (MT + 1) * 32) out_row(e / D)[e % D] = NAN;
+        return;
+    }
+    const int nstages = (L + SUBTOK - 1) / SUBTOK;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, MT);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (warp == MT) {
+        // ---- producer: lane 0 fills stage k % NST once every consumer has released it
+        if (lane != 0) return;
+        const int32_t* trow = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
+        const int bs = p.block_size, bshift = p.block_shift;
+        auto block_index = [&](int tok) { return bshift >= 0 ? (tok >> bshift) : (tok / bs); };
+        auto block_offset = [&](int tok) { return bshift >= 0 ? (tok & (bs - 1)) : (tok % bs); };
+        const uint64_t policy = l2_policy_evict_first();
+        int cur[kWideSub], nxt[kWideSub];
+        auto entries = [&](int k, int (&e)[kWideSub]) {  // table entries of stage k's tiles
+#pragma unroll
+            for (int u = 0; u < kWideSub; ++u) {
+                const int tok = k * SUBTOK + u * TT;
+                e[u] = tok < L ? __ldg(trow + block_index(tok)) : 0;
+            }
+        };
+        if (nstages > 0) entries(0, cur);
+        for (int k = 0; k < nstages; ++k) {
+            if (k + 1 < nstages) entries(k + 1, nxt);  // a stage ahead
+            const int s = k % NST;
+            if (k >= NST && !mbar_wait_bounded(empty0 + 8 * s, ((k / NST) - 1) & 1, p.wait_limit_ns)) {
+                set_error(p.err, ERR_TIMEOUT);  // the consumers' own waits give up in turn
+                return;
+            }
+            uint32_t bytes = 0;
+            int badmask = 0;
+#pragma unroll
+            for (int u = 0; u < kWideSub; ++u) {
+                if (k * SUBTOK + u * TT >= L) continue;
+                if (cur[u] >= 0 && (long long)cur[u] < p.num_blocks) bytes += 2 * SUBTILE;
+                else badmask |= 1 << u;
+            }
+            bad[s] = badmask;
+            if (badmask) set_error(p.err, ERR_BOUNDS);
+            const uint32_t full = full0 + 8 * s;
+            const uint32_t dst = smem_u32(smem) + uint32_t(s) * STAGE;
+            mbar_arrive_expect_tx(full, bytes);
+#pragma unroll
+            for (int u = 0; u < kWideSub; ++u) {
+                const int tok = k * SUBTOK + u * TT;
+                if (tok >= L || (badmask >> u) & 1) continue;
+                const int y = (cur[u] * Hkv + kvh) * bs + block_offset(tok);
+#pragma unroll
+                for (int hh = 0; hh < HALVES; ++hh) {
+                    tma_load_2d(dst + u * SUBTILE + hh * HALF, &tmap_k, hh * 64, y, full, policy);
+                    tma_load_2d(dst + KV + u * SUBTILE + hh * HALF, &tmap_v, hh * 64, y, full, policy);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kWideSub; ++u) cur[u] = nxt[u];
+        }
+        return;
+    }
+
+    // ---- consumer warp: query rows r0 = 16 * warp + g and r1 = r0 + 8 (zero rows past RR)
+    const int g = lane >> 2, t = lane & 3;
+    const int r0 = 16 * warp + g, r1 = r0 + 8;
+    auto qrow = [&](int r) -> const uint16_t* {
+        const int j = r / G, h = r - (r / G) * G;
+        return p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D;
+    };
+    uint32_t qa[KSTEPS][4];
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+        const int c = ks * 16 + 2 * t;
+        qa[ks][0] = r0 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r0) + c)) : 0u;
+        qa[ks][1] = r1 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r1) + c)) : 0u;
+        qa[ks][2] = r0 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r0) + c + 8)) : 0u;
+        qa[ks][3] = r1 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r1) + c + 8)) : 0u;
+    }
+    // tokens t < lim are visible to a row; padding rows see nothing
+    const int lim0 = r0 < RR ? L - Q + r0 / G + 1 : 0;
+    const int lim1 = r1 < RR ? L - Q + r1 / G + 1 : 0;
+
+    float o[NTD][4];
+#pragma unroll
+    for (int n = 0; n < NTD; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    // swizzled byte offset of 16-byte chunk c (0 .. D/8-1) of token row `tok` in a tile
+    auto swz = [](int tok, int c) { return (c >> 3) * HALF + tok * 128 + (((c & 7) ^ (tok & 7)) << 4); };
+
+    bool timed_out = false, failed = false;
+    int k = 0;
+    for (; k < nstages; ++k) {
+        const int s = k % NST;
+        const bool ok = mbar_wait_bounded(full0 + 8 * s, (k / NST) & 1, p.wait_limit_ns);
+        if (__any_sync(FULL_MASK, !ok)) { timed_out = true; break; }
+        if (bad[s]) failed = true;  // a tile without its copy: the rows end up NaN
+        unsigned char* Kst = smem + size_t(s) * STAGE;
+        unsigned char* Vst = Kst + KV;
+        const int tok_base = k * SUBTOK;
+        const int nv = min(SUBTOK, L - tok_base);          // valid tokens of the stage
+        const int nsub = (nv + TT - 1) / TT;
+        if (nv < nsub * TT) {
+            // rows past the sequence in its last tile hold other data (or poison): zero V
+            // there so 0 * V stays 0.  Every consumer writes the same zeros before reading.
+            unsigned char* Vl = Vst + (nsub - 1) * SUBTILE;
+            const int r_first = nv - (nsub - 1) * TT;
+            for (int b = lane; b < (TT - r_first) * HALVES * 8; b += 32) {
+                const int row = r_first + b / (HALVES * 8), rest = b % (HALVES * 8);
+                *reinterpret_cast<uint4*>(Vl + (rest >> 3) * HALF + row * 128 + (rest & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before the stage's next TMA fill
+            __syncwarp();
+        }
+        for (int u = 0; u < nsub; ++u) {
+            const uint32_t ks_addr = smem_u32(Kst + u * SUBTILE), vs_addr = smem_u32(Vst + u * SUBTILE);
+            const int tok0 = tok_base + u * TT;
+            // -- S = Q K^T for the 16 tokens: two n-tiles of 8
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kp = 0; kp < KSTEPS / 2; ++kp) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int tok = nt * 8 + (lane & 7);
+                    const int c = kp * 4 + (lane >> 3);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(ks_addr + swz(tok, c), b0, b1, b2, b3);
+                    mma_bf16_16816(sc[nt], qa[2 * kp], b0, b1);
+                    mma_bf16_16816(sc[nt], qa[2 * kp + 1], b2, b3);
+                }
+            }
+            // -- mask, scale to base 2, online softmax per row (the 4 lanes of a quad share a row)
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = tok0 + nt * 8 + 2 * t + (e & 1);
+                    const bool vis = tok < (e < 2 ? lim0 : lim1);
+                    sc[nt][e] = vis ? sc[nt][e] * p.scale_log2 : -INFINITY;
+                    if (e < 2) mx0 = fmaxf(mx0, sc[nt][e]); else mx1 = fmaxf(mx1, sc[nt][e]);
+                }
+#pragma unroll
+            for (int off = 1; off <= 2; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float sf0 = mn0 == -INFINITY ? 0.f : mn0, sf1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = exp2_approx(m0 - sf0), al1 = exp2_approx(m1 - sf1);
+            m0 = mn0;
+            m1 = mn1;
+            float pr[2][4];
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    pr[nt][e] = exp2_approx(sc[nt][e] - (e < 2 ? sf0 : sf1));
+                    if (e < 2) ps0 += pr[nt][e]; else ps1 += pr[nt][e];
+                }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+#pragma unroll
+            for (int n = 0; n < NTD; ++n) {
+                o[n][0] *= al0; o[n][1] *= al0;
+                o[n][2] *= al1; o[n][3] *= al1;
+            }
+            // -- P as A fragments, split into bf16 hi + lo
+            uint32_t ph[4], pl[4];
+            {
+                const float* v[4] = {&pr[0][0], &pr[0][2], &pr[1][0], &pr[1][2]};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float a = v[i][0], b = v[i][1];
+                    ph[i] = pack_bf16x2(a, b);
+                    const float ah = __uint_as_float(ph[i] << 16), bh = __uint_as_float(ph[i] & 0xffff0000u);
+                    pl[i] = pack_bf16x2(a - ah, b - bh);
+                }
+            }
+            // -- O += P V: V fragments via ldmatrix.trans, two n-tiles of 8 dims per load
+#pragma unroll
+            for (int dp = 0; dp < NTD / 2; ++dp) {
+                const int mi = lane >> 3;
+                const int tok = ((mi & 1) << 3) + (lane & 7);
+                const int c = 2 * dp + (mi >> 1);
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(vs_addr + swz(tok, c), v0, v1, v2, v3);
+                mma_bf16_16816(o[2 * dp], ph, v0, v1);
+                mma_bf16_16816(o[2 * dp], pl, v0, v1);
+                mma_bf16_16816(o[2 * dp + 1], ph, v2, v3);
+                mma_bf16_16816(o[2 * dp + 1], pl, v2, v3);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);  // this warp is done with the stage
+    }
+    if (timed_out) {
+        // the producer may still have fills of the next stages in flight: give them a
+        // bounded chance to land before the CTA's shared memory goes away
+        if (lane == 0) set_error(p.err, ERR_TIMEOUT);
+        const int last = min(k + NST, nstages);
+        for (int kk = k; kk < last; ++kk) mbar_wait_bounded(full0 + 8 * (kk % NST), (kk / NST) & 1, p.wait_limit_ns);
+        failed = true;
+    }
+
+    // ---- row sums over the quad, then this warp's rows
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+        l0 += __shfl_xor_sync(FULL_MASK, l0, off);
+        l1 += __shfl_xor_sync(FULL_MASK, l1, off);
+    }
+    const float i0 = l0 == 0.f ? 0.f : 1.f / l0, i1 = l1 == 0.f ? 0.f : 1.f / l1;  // no token: 0
+#pragma unroll
+    for (int n = 0; n < NTD; ++n) {
+        const int d = n * 8 + 2 * t;
+        if (r0 < RR)
+            *reinterpret_cast<float2*>(out_row(r0) + d) =
+                failed ? make_float2(NAN, NAN) : make_float2(o[n][0] * i0, o[n][1] * i0);
+        if (r1 < RR)
+            *reinterpret_cast<float2*>(out_row(r1) + d) =
+                failed ? make_float2(NAN, NAN) : make_float2(o[n][2] * i1, o[n][3] * i1);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -395,6 +686,37 @@ static cudaError_t launch_multi(const CUtensorMap& mk, const CUtensorMap& mv, co
     return cudaGetLastError();
 }
 
+template <int D, int MT>
+static cudaError_t launch_multi_wide(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p,
+                                     cudaStream_t stream) {
+    using Lay = WideLayout<D, kWideStages>;
+    auto kern = paged_multi_query_wide_kernel<D, MT, kWideStages>;
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit == 0 || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Lay::ALLOC));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const long long grid = (long long)p.num_seqs * p.num_kv_heads;
+    kern<<<unsigned(grid), (MT + 1) * 32, Lay::ALLOC, stream>>>(mk, mv, p);
+    return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_multi_any(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p,
+                                    cudaStream_t stream) {
+    if (p.rows <= kMultiMaxRows) return launch_multi<D>(mk, mv, p, stream);
+    switch ((p.rows + 15) / 16) {
+        case 2: return launch_multi_wide<D, 2>(mk, mv, p, stream);
+        case 3: return launch_multi_wide<D, 3>(mk, mv, p, stream);
+        default: return launch_multi_wide<D, 4>(mk, mv, p, stream);
+    }
+}
+
 }  // namespace pf
 
 using namespace pf;
@@ -412,7 +734,7 @@ extern "C" pf_status pf_paged_attention_multi_query(const void* q, const void* k
     const int group = num_q_heads / num_kv_heads;
     if (head_dim != 64 && head_dim != 128) return PF_ERR_UNSUPPORTED;
     if (block_size % kTileTokens != 0) return PF_ERR_UNSUPPORTED;
-    if ((long long)group * q_len > kMultiMaxRows) return PF_ERR_UNSUPPORTED;
+    if ((long long)group * q_len > kWideMaxRows) return PF_ERR_UNSUPPORTED;
     const long long rows = num_blocks * num_kv_heads * (long long)block_size;
     if (rows > INT32_MAX || (long long)num_seqs * num_kv_heads > INT32_MAX) return PF_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PF_OK;
@@ -443,7 +765,7 @@ extern "C" pf_status pf_paged_attention_multi_query(const void* q, const void* k
     p.block_size = block_size;
     p.block_shift = (block_size & (block_size - 1)) == 0 ? __builtin_ctz(unsigned(block_size)) : -1;
     p.max_blocks_per_seq = max_blocks_per_seq;
-    const cudaError_t e = head_dim == 64 ? launch_multi<64>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream))
-                                         : launch_multi<128>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
+    const cudaError_t e = head_dim == 64 ? launch_multi_any<64>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream))
+                                         : launch_multi_any<128>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }
