@@ -342,8 +342,11 @@ __global__ void __launch_bounds__(NW * 32) paged_multi_query_kernel(const __grid
 //
 // More than 16 query rows per kv head (g * q_len up to 64: e.g. 16 draft tokens at
 // g = 4, or a 64-token prompt chunk of a multi-head model).  One CTA per
-// (sequence, kv head) with MT consumer warps, warp w owning query rows
-// [16w, 16w + 16) as one m16 tile, and one producer warp.  The producer's lane 0
+// (sequence, kv head) with MT x NG consumer warps -- warp w owns query rows
+// [16 mt, 16 mt + 16), mt = w % MT, as one m16 tile, and takes the stages
+// k = grp, grp + NG, ... of its group grp = w / MT -- and one producer warp.  With
+// 32 rows or fewer two groups split the stages (four consumer warps, like the
+// 16-row kernel's token split) and merge their (m, l, O) at the end.  The producer's lane 0
 // streams the sequence in stages of 64 tokens (four 16-token tiles, K and V, by TMA
 // tensor copies with the 128-byte swizzle) through an NST-deep ring shared by all
 // consumers: a "full" mbarrier per stage completes when its bytes land, an "empty"
@@ -368,8 +371,8 @@ struct WideLayout {
     static constexpr size_t ALLOC = BYTES + 1024;           // room to align to 1024
 };
 
-template <int D, int MT, int NST>
-__global__ void __launch_bounds__((MT + 1) * 32) paged_multi_query_wide_kernel(
+template <int D, int MT, int NG, int NST>
+__global__ void __launch_bounds__((MT * NG + 1) * 32) paged_multi_query_wide_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v, const MultiParams p) {
     using Lay = WideLayout<D, NST>;
     constexpr int TT = Lay::TT, HALVES = Lay::HALVES, HALF = Lay::HALF_BYTES, SUBTILE = Lay::SUBTILE;
@@ -377,6 +380,7 @@ __global__ void __launch_bounds__((MT + 1) * 32) paged_multi_query_wide_kernel(
     constexpr int SUBTOK = kWideSub * TT;  // tokens per stage
     constexpr int KSTEPS = D / 16;         // k-steps of S = Q K^T
     constexpr int NTD = D / 8;             // n-tiles of O = P V
+    constexpr int NC = MT * NG;            // consumer warps; warp NC is the producer
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -395,7 +399,7 @@ __global__ void __launch_bounds__((MT + 1) * 32) paged_multi_query_wide_kernel(
     };
     if (len_bad) {
         if (threadIdx.x == 0) set_error(p.err, ERR_BOUNDS);
-        for (int e = threadIdx.x; e < RR * D; e += (MT + 1) * 32) out_row(e / D)[e % D] = NAN;
+        for (int e = threadIdx.x; e < RR * D; e += (NC + 1) * 32) out_row(e / D)[e % D] = NAN;
         return;
     }
     const int nstages = (L + SUBTOK - 1) / SUBTOK;
@@ -409,8 +413,8 @@ __global__ void __launch_bounds__((MT + 1) * 32) paged_multi_query_wide_kernel(
     }
     __syncthreads();
 
-    if (warp == MT) {
-        // ---- producer: lane 0 fills stage k % NST once every consumer has released it
+    if (warp == NC) {
+        // ---- producer: lane 0 fills stage k % NST once its consumers have released it
         if (lane != 0) return;
         const int32_t* trow = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
         const int bs = p.block_size, bshift = p.block_shift;
@@ -463,9 +467,11 @@ __global__ void __launch_bounds__((MT + 1) * 32) paged_multi_query_wide_kernel(
         return;
     }
 
-    // ---- consumer warp: query rows r0 = 16 * warp + g and r1 = r0 + 8 (zero rows past RR)
+    // ---- consumer warp: m-tile mt (query rows r0 = 16 mt + g and r1 = r0 + 8, zero rows past
+    // RR) over the stages of its group, k = grp, grp + NG, ...
+    const int mt = warp % MT, grp = warp / MT;
     const int g = lane >> 2, t = lane & 3;
-    const int r0 = 16 * warp + g, r1 = r0 + 8;
+    const int r0 = 16 * mt + g, r1 = r0 + 8;
     auto qrow = [&](int r) -> const uint16_t* {
         const int j = r / G, h = r - (r / G) * G;
         return p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D;
@@ -492,8 +498,8 @@ __global__ void __launch_bounds__((MT + 1) * 32) paged_multi_query_wide_kernel(
     auto swz = [](int tok, int c) { return (c >> 3) * HALF + tok * 128 + (((c & 7) ^ (tok & 7)) << 4); };
 
     bool timed_out = false, failed = false;
-    int k = 0;
-    for (; k < nstages; ++k) {
+    int k = grp;
+    for (; k < nstages; k += NG) {
         const int s = k % NST;
         const bool ok = mbar_wait_bounded(full0 + 8 * s, (k / NST) & 1, p.wait_limit_ns);
         if (__any_sync(FULL_MASK, !ok)) { timed_out = true; break; }
@@ -608,12 +614,57 @@ __global__ void __launch_bounds__((MT + 1) * 32) paged_multi_query_wide_kernel(
         failed = true;
     }
 
-    // ---- row sums over the quad, then this warp's rows
+    // ---- row sums over the quad
 #pragma unroll
     for (int off = 1; off <= 2; off <<= 1) {
         l0 += __shfl_xor_sync(FULL_MASK, l0, off);
         l1 += __shfl_xor_sync(FULL_MASK, l1, off);
     }
+    if constexpr (NG > 1) {
+        // ---- the groups' partial (m, l, O) of an m-tile meet in the stage memory, free once
+        // every consumer is past its last stage (named barrier of the consumers only)
+        asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
+        constexpr int SLOT = 16 * D + 64;  // floats: O [16][D], then m, l of the 16 rows, failed
+        float* mine = reinterpret_cast<float*>(smem) + size_t(warp) * SLOT;
+        if (grp > 0) {
+#pragma unroll
+            for (int n = 0; n < NTD; ++n) {
+                *reinterpret_cast<float2*>(mine + g * D + n * 8 + 2 * t) = make_float2(o[n][0], o[n][1]);
+                *reinterpret_cast<float2*>(mine + (g + 8) * D + n * 8 + 2 * t) = make_float2(o[n][2], o[n][3]);
+            }
+            if (t == 0) {
+                mine[16 * D + g] = m0; mine[16 * D + g + 8] = m1;
+                mine[16 * D + 16 + g] = l0; mine[16 * D + 16 + g + 8] = l1;
+            }
+            if (lane == 0) mine[16 * D + 32] = failed ? 1.f : 0.f;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
+        if (grp > 0) return;
+#pragma unroll
+        for (int gi = 1; gi < NG; ++gi) {
+            const float* other = reinterpret_cast<const float*>(smem) + size_t(gi * MT + mt) * SLOT;
+            if (other[16 * D + 32] != 0.f) failed = true;
+            const float mo0 = other[16 * D + g], mo1 = other[16 * D + g + 8];
+            const float lo0 = other[16 * D + 16 + g], lo1 = other[16 * D + 16 + g + 8];
+            const float M0 = fmaxf(m0, mo0), M1 = fmaxf(m1, mo1);
+            const float s0 = M0 == -INFINITY ? 0.f : M0, s1 = M1 == -INFINITY ? 0.f : M1;
+            const float a0 = exp2_approx(m0 - s0), b0 = exp2_approx(mo0 - s0);
+            const float a1 = exp2_approx(m1 - s1), b1 = exp2_approx(mo1 - s1);
+#pragma unroll
+            for (int n = 0; n < NTD; ++n) {
+                const float2 x0 = *reinterpret_cast<const float2*>(other + g * D + n * 8 + 2 * t);
+                const float2 x1 = *reinterpret_cast<const float2*>(other + (g + 8) * D + n * 8 + 2 * t);
+                o[n][0] = o[n][0] * a0 + x0.x * b0; o[n][1] = o[n][1] * a0 + x0.y * b0;
+                o[n][2] = o[n][2] * a1 + x1.x * b1; o[n][3] = o[n][3] * a1 + x1.y * b1;
+            }
+            l0 = l0 * a0 + lo0 * b0;
+            l1 = l1 * a1 + lo1 * b1;
+            m0 = M0;
+            m1 = M1;
+        }
+    }
+
+    // ---- this warp's rows
     const float i0 = l0 == 0.f ? 0.f : 1.f / l0, i1 = l1 == 0.f ? 0.f : 1.f / l1;  // no token: 0
 #pragma unroll
     for (int n = 0; n < NTD; ++n) {
@@ -686,11 +737,11 @@ static cudaError_t launch_multi(const CUtensorMap& mk, const CUtensorMap& mv, co
     return cudaGetLastError();
 }
 
-template <int D, int MT>
+template <int D, int MT, int NG>
 static cudaError_t launch_multi_wide(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p,
                                      cudaStream_t stream) {
     using Lay = WideLayout<D, kWideStages>;
-    auto kern = paged_multi_query_wide_kernel<D, MT, kWideStages>;
+    auto kern = paged_multi_query_wide_kernel<D, MT, NG, kWideStages>;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -702,7 +753,7 @@ static cudaError_t launch_multi_wide(const CUtensorMap& mk, const CUtensorMap& m
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     const long long grid = (long long)p.num_seqs * p.num_kv_heads;
-    kern<<<unsigned(grid), (MT + 1) * 32, Lay::ALLOC, stream>>>(mk, mv, p);
+    kern<<<unsigned(grid), (MT * NG + 1) * 32, Lay::ALLOC, stream>>>(mk, mv, p);
     return cudaGetLastError();
 }
 
@@ -711,9 +762,9 @@ static cudaError_t launch_multi_any(const CUtensorMap& mk, const CUtensorMap& mv
                                     cudaStream_t stream) {
     if (p.rows <= kMultiMaxRows) return launch_multi<D>(mk, mv, p, stream);
     switch ((p.rows + 15) / 16) {
-        case 2: return launch_multi_wide<D, 2>(mk, mv, p, stream);
-        case 3: return launch_multi_wide<D, 3>(mk, mv, p, stream);
-        default: return launch_multi_wide<D, 4>(mk, mv, p, stream);
+        case 2: return launch_multi_wide<D, 2, 2>(mk, mv, p, stream);   // two groups take alternate stages
+        case 3: return launch_multi_wide<D, 3, 1>(mk, mv, p, stream);
+        default: return launch_multi_wide<D, 4, 1>(mk, mv, p, stream);
     }
 }
 
