@@ -27,6 +27,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include <cuda.h>  // CUtensorMap and its enums only; the encoder is fetched from the runtime
 #include <cuda_runtime.h>
@@ -372,7 +373,7 @@ struct WideLayout {
 };
 
 template <int D, int MT, int NG, int NST>
-__global__ void __launch_bounds__((MT * NG + 1) * 32) paged_multi_query_wide_kernel(
+__global__ void __launch_bounds__((MT * NG + 1) * 32, 2) paged_multi_query_wide_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v, const MultiParams p) {
     using Lay = WideLayout<D, NST>;
     constexpr int TT = Lay::TT, HALVES = Lay::HALVES, HALF = Lay::HALF_BYTES, SUBTILE = Lay::SUBTILE;
@@ -381,6 +382,7 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32) paged_multi_query_wide_ker
     constexpr int KSTEPS = D / 16;         // k-steps of S = Q K^T
     constexpr int NTD = D / 8;             // n-tiles of O = P V
     constexpr int NC = MT * NG;            // consumer warps; warp NC is the producer
+    constexpr bool PAIRS = NG > 1;
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -522,32 +524,43 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32) paged_multi_query_wide_ker
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before the stage's next TMA fill
             __syncwarp();
         }
-        for (int u = 0; u < nsub; ++u) {
-            const uint32_t ks_addr = smem_u32(Kst + u * SUBTILE), vs_addr = smem_u32(Vst + u * SUBTILE);
+        // tiles u .. u + NS - 1 of the stage per softmax step: NS = 2 where the registers allow
+        // it (two warp groups), else 1
+        auto step = [&](auto ns_const, int u) {
+            constexpr int NS = decltype(ns_const)::value;
+            constexpr int NT = 2 * NS;  // n-tiles of 8 tokens
             const int tok0 = tok_base + u * TT;
-            // -- S = Q K^T for the 16 tokens: two n-tiles of 8
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            // -- S = Q K^T (with two warp groups the k-steps alternate between two accumulator
+            // chains; the 64-row variant has no registers for the second chain)
+            float sa[NT][4], sb[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
 #pragma unroll
             for (int kp = 0; kp < KSTEPS / 2; ++kp) {
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int tok = nt * 8 + (lane & 7);
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int tok = (nt & 1) * 8 + (lane & 7);
                     const int c = kp * 4 + (lane >> 3);
                     uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(ks_addr + swz(tok, c), b0, b1, b2, b3);
-                    mma_bf16_16816(sc[nt], qa[2 * kp], b0, b1);
-                    mma_bf16_16816(sc[nt], qa[2 * kp + 1], b2, b3);
+                    ldmatrix_x4(smem_u32(Kst + (u + nt / 2) * SUBTILE) + swz(tok, c), b0, b1, b2, b3);
+                    mma_bf16_16816(sa[nt], qa[2 * kp], b0, b1);
+                    if constexpr (PAIRS) mma_bf16_16816(sb[nt], qa[2 * kp + 1], b2, b3);
+                    else mma_bf16_16816(sa[nt], qa[2 * kp + 1], b2, b3);
                 }
             }
             // -- mask, scale to base 2, online softmax per row (the 4 lanes of a quad share a row)
+            float sc[NT][4];
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int tok = tok0 + nt * 8 + 2 * t + (e & 1);
                     const bool vis = tok < (e < 2 ? lim0 : lim1);
-                    sc[nt][e] = vis ? sc[nt][e] * p.scale_log2 : -INFINITY;
+                    const float dot = PAIRS ? sa[nt][e] + sb[nt][e] : sa[nt][e];
+                    sc[nt][e] = vis ? dot * p.scale_log2 : -INFINITY;
                     if (e < 2) mx0 = fmaxf(mx0, sc[nt][e]); else mx1 = fmaxf(mx1, sc[nt][e]);
                 }
 #pragma unroll
@@ -560,14 +573,13 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32) paged_multi_query_wide_ker
             const float al0 = exp2_approx(m0 - sf0), al1 = exp2_approx(m1 - sf1);
             m0 = mn0;
             m1 = mn1;
-            float pr[2][4];
             float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    pr[nt][e] = exp2_approx(sc[nt][e] - (e < 2 ? sf0 : sf1));
-                    if (e < 2) ps0 += pr[nt][e]; else ps1 += pr[nt][e];
+                    sc[nt][e] = exp2_approx(sc[nt][e] - (e < 2 ? sf0 : sf1));  // now the probability
+                    if (e < 2) ps0 += sc[nt][e]; else ps1 += sc[nt][e];
                 }
             l0 = l0 * al0 + ps0;
             l1 = l1 * al1 + ps1;
@@ -576,32 +588,41 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32) paged_multi_query_wide_ker
                 o[n][0] *= al0; o[n][1] *= al0;
                 o[n][2] *= al1; o[n][3] *= al1;
             }
-            // -- P as A fragments, split into bf16 hi + lo
-            uint32_t ph[4], pl[4];
-            {
-                const float* v[4] = {&pr[0][0], &pr[0][2], &pr[1][0], &pr[1][2]};
+            // -- P of each 16-token tile as A fragments, split into bf16 hi + lo
+            uint32_t ph[NS][4], pl[NS][4];
+#pragma unroll
+            for (int s2 = 0; s2 < NS; ++s2) {
+                const float* v[4] = {&sc[2 * s2][0], &sc[2 * s2][2], &sc[2 * s2 + 1][0], &sc[2 * s2 + 1][2]};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float a = v[i][0], b = v[i][1];
-                    ph[i] = pack_bf16x2(a, b);
-                    const float ah = __uint_as_float(ph[i] << 16), bh = __uint_as_float(ph[i] & 0xffff0000u);
-                    pl[i] = pack_bf16x2(a - ah, b - bh);
+                    ph[s2][i] = pack_bf16x2(a, b);
+                    const float ah = __uint_as_float(ph[s2][i] << 16), bh = __uint_as_float(ph[s2][i] & 0xffff0000u);
+                    pl[s2][i] = pack_bf16x2(a - ah, b - bh);
                 }
             }
             // -- O += P V: V fragments via ldmatrix.trans, two n-tiles of 8 dims per load
 #pragma unroll
             for (int dp = 0; dp < NTD / 2; ++dp) {
-                const int mi = lane >> 3;
-                const int tok = ((mi & 1) << 3) + (lane & 7);
-                const int c = 2 * dp + (mi >> 1);
-                uint32_t v0, v1, v2, v3;
-                ldmatrix_x4_trans(vs_addr + swz(tok, c), v0, v1, v2, v3);
-                mma_bf16_16816(o[2 * dp], ph, v0, v1);
-                mma_bf16_16816(o[2 * dp], pl, v0, v1);
-                mma_bf16_16816(o[2 * dp + 1], ph, v2, v3);
-                mma_bf16_16816(o[2 * dp + 1], pl, v2, v3);
+#pragma unroll
+                for (int s2 = 0; s2 < NS; ++s2) {
+                    const int mi = lane >> 3;
+                    const int tok = ((mi & 1) << 3) + (lane & 7);
+                    const int c = 2 * dp + (mi >> 1);
+                    uint32_t v0, v1, v2, v3;
+                    ldmatrix_x4_trans(smem_u32(Vst + (u + s2) * SUBTILE) + swz(tok, c), v0, v1, v2, v3);
+                    mma_bf16_16816(o[2 * dp], ph[s2], v0, v1);
+                    mma_bf16_16816(o[2 * dp], pl[s2], v0, v1);
+                    mma_bf16_16816(o[2 * dp + 1], ph[s2], v2, v3);
+                    mma_bf16_16816(o[2 * dp + 1], pl[s2], v2, v3);
+                }
             }
+        };
+        int u = 0;
+        if constexpr (PAIRS) {
+            for (; u + 1 < nsub; u += 2) step(std::integral_constant<int, 2>{}, u);
         }
+        for (; u < nsub; ++u) step(std::integral_constant<int, 1>{}, u);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);  // this warp is done with the stage
     }
