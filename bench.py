@@ -513,7 +513,7 @@ def main():
     extras = {}
     if not args.no_extras and rank == 0:
         g = wl.num_q_heads // wl.num_kv_heads
-        for q_len in (4, 8, 16):
+        for q_len in (4, 8, 12, 16):
             if runner.split or g * q_len > 64:
                 continue
             # the same resident cache, with the last q_len tokens of every sequence as new (draft) tokens

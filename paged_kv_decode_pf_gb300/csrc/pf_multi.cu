@@ -354,10 +354,30 @@ __global__ void __launch_bounds__(NW * 32) paged_multi_query_kernel(const __grid
 // one when every consumer has read it.  Each consumer runs the same per-tile
 // arithmetic as the 16-row kernel on its rows and writes them itself.
 constexpr int kWideMaxRows = 64;
+// per variant (2, 3 or 4 m-tiles): ring depth, and the options of the kernel (OPT bits
+// below: query rows in shared memory, two tiles per softmax step, two score chains)
+#ifndef PF_WIDE_NST_2
+#define PF_WIDE_NST_2 3
+#endif
+#ifndef PF_WIDE_OPT_2
+#define PF_WIDE_OPT_2 2
+#endif
+#ifndef PF_WIDE_NST_3
+#define PF_WIDE_NST_3 2
+#endif
+#ifndef PF_WIDE_OPT_3
+#define PF_WIDE_OPT_3 3
+#endif
+#ifndef PF_WIDE_NST_4
+#define PF_WIDE_NST_4 2
+#endif
+#ifndef PF_WIDE_OPT_4
+#define PF_WIDE_OPT_4 3
+#endif
 constexpr int kWideSub = 4;     // 16-token tiles per stage
 constexpr int kWideStages = 3;
 
-template <int D, int NST>
+template <int D, int NST, int NC = 0>
 struct WideLayout {
     static constexpr int TT = kTileTokens;
     static constexpr int HALVES = D / 64;
@@ -368,21 +388,31 @@ struct WideLayout {
     static constexpr size_t FULL = size_t(NST) * STAGE;     // NST mbarriers
     static constexpr size_t EMPTY = FULL + size_t(NST) * 8;  // NST mbarriers
     static constexpr size_t BAD = EMPTY + size_t(NST) * 8;   // NST ints: bit u = tile u had no copy
-    static constexpr size_t BYTES = BAD + ((NST * 4 + 15) / 16) * 16;
+    // query rows in shared memory (when the registers are short): per consumer warp 16 rows
+    // of D bf16, rows padded by 16 bytes so the ldmatrix reads are free of bank conflicts
+    static constexpr int QSTRIDE = D * 2 + 16;
+    static constexpr size_t QAREA = BAD + ((NST * 4 + 15) / 16) * 16;
+    static constexpr size_t BYTES = QAREA + size_t(NC) * 16 * QSTRIDE;
     static constexpr size_t ALLOC = BYTES + 1024;           // room to align to 1024
 };
 
-template <int D, int MT, int NG, int NST>
+// OPT bits: kWideQs (query rows in shared memory), kWidePairs (two tiles per softmax
+// step), kWideSplit (two score accumulator chains)
+constexpr int kWideQs = 1, kWidePairs = 2, kWideSplit = 4;
+
+template <int D, int MT, int NG, int NST, int OPT>
 __global__ void __launch_bounds__((MT * NG + 1) * 32, 2) paged_multi_query_wide_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v, const MultiParams p) {
-    using Lay = WideLayout<D, NST>;
+    constexpr bool QS = (OPT & kWideQs) != 0;
+    using Lay = WideLayout<D, NST, QS ? MT * NG : 0>;
     constexpr int TT = Lay::TT, HALVES = Lay::HALVES, HALF = Lay::HALF_BYTES, SUBTILE = Lay::SUBTILE;
     constexpr int KV = Lay::KV, STAGE = Lay::STAGE;
     constexpr int SUBTOK = kWideSub * TT;  // tokens per stage
     constexpr int KSTEPS = D / 16;         // k-steps of S = Q K^T
     constexpr int NTD = D / 8;             // n-tiles of O = P V
     constexpr int NC = MT * NG;            // consumer warps; warp NC is the producer
-    constexpr bool PAIRS = NG > 1;
+    constexpr bool PAIRS = (OPT & kWidePairs) != 0;
+    constexpr bool SPLIT = (OPT & kWideSplit) != 0;
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -478,15 +508,37 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32, 2) paged_multi_query_wide_
         const int j = r / G, h = r - (r / G) * G;
         return p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D;
     };
-    uint32_t qa[KSTEPS][4];
+    // Q as mma A fragments of k-step ks: held in registers, or (QS) read from this warp's
+    // 16 rows in shared memory by ldmatrix at each use
+    uint32_t qa[QS ? 1 : KSTEPS][4];
+    const uint32_t qbase = smem_u32(smem + Lay::QAREA) + uint32_t(warp) * 16 * Lay::QSTRIDE;
+    if constexpr (QS) {
+        unsigned char* qs = smem + Lay::QAREA + size_t(warp) * 16 * Lay::QSTRIDE;
+        for (int e = lane; e < 16 * (D / 8); e += 32) {
+            const int rr = e / (D / 8), ch = e % (D / 8), r = 16 * mt + rr;
+            const uint4 v = r < RR ? __ldg(reinterpret_cast<const uint4*>(qrow(r)) + ch) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(qs + rr * Lay::QSTRIDE + ch * 16) = v;
+        }
+        __syncwarp();
+    } else {
 #pragma unroll
-    for (int ks = 0; ks < KSTEPS; ++ks) {
-        const int c = ks * 16 + 2 * t;
-        qa[ks][0] = r0 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r0) + c)) : 0u;
-        qa[ks][1] = r1 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r1) + c)) : 0u;
-        qa[ks][2] = r0 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r0) + c + 8)) : 0u;
-        qa[ks][3] = r1 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r1) + c + 8)) : 0u;
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+            const int c = ks * 16 + 2 * t;
+            qa[ks][0] = r0 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r0) + c)) : 0u;
+            qa[ks][1] = r1 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r1) + c)) : 0u;
+            qa[ks][2] = r0 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r0) + c + 8)) : 0u;
+            qa[ks][3] = r1 < RR ? __ldg(reinterpret_cast<const uint32_t*>(qrow(r1) + c + 8)) : 0u;
+        }
     }
+    auto q_frag = [&](int ks, uint32_t (&a)[4]) {
+        if constexpr (QS) {
+            ldmatrix_x4(qbase + uint32_t((lane & 15) * Lay::QSTRIDE + (ks * 16 + (lane >> 4) * 8) * 2), a[0], a[1],
+                        a[2], a[3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = qa[ks][i];
+        }
+    };
     // tokens t < lim are visible to a row; padding rows see nothing
     const int lim0 = r0 < RR ? L - Q + r0 / G + 1 : 0;
     const int lim1 = r1 < RR ? L - Q + r1 / G + 1 : 0;
@@ -539,15 +591,18 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32, 2) paged_multi_query_wide_
                 for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
 #pragma unroll
             for (int kp = 0; kp < KSTEPS / 2; ++kp) {
+                uint32_t qlo[4], qhi[4];
+                q_frag(2 * kp, qlo);
+                q_frag(2 * kp + 1, qhi);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int tok = (nt & 1) * 8 + (lane & 7);
                     const int c = kp * 4 + (lane >> 3);
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4(smem_u32(Kst + (u + nt / 2) * SUBTILE) + swz(tok, c), b0, b1, b2, b3);
-                    mma_bf16_16816(sa[nt], qa[2 * kp], b0, b1);
-                    if constexpr (PAIRS) mma_bf16_16816(sb[nt], qa[2 * kp + 1], b2, b3);
-                    else mma_bf16_16816(sa[nt], qa[2 * kp + 1], b2, b3);
+                    mma_bf16_16816(sa[nt], qlo, b0, b1);
+                    if constexpr (SPLIT) mma_bf16_16816(sb[nt], qhi, b2, b3);
+                    else mma_bf16_16816(sa[nt], qhi, b2, b3);
                 }
             }
             // -- mask, scale to base 2, online softmax per row (the 4 lanes of a quad share a row)
@@ -559,7 +614,7 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32, 2) paged_multi_query_wide_
                 for (int e = 0; e < 4; ++e) {
                     const int tok = tok0 + nt * 8 + 2 * t + (e & 1);
                     const bool vis = tok < (e < 2 ? lim0 : lim1);
-                    const float dot = PAIRS ? sa[nt][e] + sb[nt][e] : sa[nt][e];
+                    const float dot = SPLIT ? sa[nt][e] + sb[nt][e] : sa[nt][e];
                     sc[nt][e] = vis ? dot * p.scale_log2 : -INFINITY;
                     if (e < 2) mx0 = fmaxf(mx0, sc[nt][e]); else mx1 = fmaxf(mx1, sc[nt][e]);
                 }
@@ -758,11 +813,11 @@ static cudaError_t launch_multi(const CUtensorMap& mk, const CUtensorMap& mv, co
     return cudaGetLastError();
 }
 
-template <int D, int MT, int NG>
+template <int D, int MT, int NG, int NST, int OPT>
 static cudaError_t launch_multi_wide(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p,
                                      cudaStream_t stream) {
-    using Lay = WideLayout<D, kWideStages>;
-    auto kern = paged_multi_query_wide_kernel<D, MT, NG, kWideStages>;
+    using Lay = WideLayout<D, NST, (OPT & kWideQs) ? MT * NG : 0>;
+    auto kern = paged_multi_query_wide_kernel<D, MT, NG, NST, OPT>;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -783,9 +838,9 @@ static cudaError_t launch_multi_any(const CUtensorMap& mk, const CUtensorMap& mv
                                     cudaStream_t stream) {
     if (p.rows <= kMultiMaxRows) return launch_multi<D>(mk, mv, p, stream);
     switch ((p.rows + 15) / 16) {
-        case 2: return launch_multi_wide<D, 2, 2>(mk, mv, p, stream);   // two groups take alternate stages
-        case 3: return launch_multi_wide<D, 3, 1>(mk, mv, p, stream);
-        default: return launch_multi_wide<D, 4, 1>(mk, mv, p, stream);
+        case 2: return launch_multi_wide<D, 2, 2, PF_WIDE_NST_2, PF_WIDE_OPT_2>(mk, mv, p, stream);  // two groups
+        case 3: return launch_multi_wide<D, 3, 1, PF_WIDE_NST_3, PF_WIDE_OPT_3>(mk, mv, p, stream);
+        default: return launch_multi_wide<D, 4, 1, PF_WIDE_NST_4, PF_WIDE_OPT_4>(mk, mv, p, stream);
     }
 }
 
