@@ -184,13 +184,20 @@ class Runner:
         if self.append:
             self.nk, self.nv = bf(wl.new_k), bf(wl.new_v)
             self.sm = torch.from_numpy(wl.slot_mapping).to(dev)
-        self.split = variant == "split" or wl.partition_size is not None
+        self.auto = variant == "auto"  # pf_paged_attention_decode_auto with the true longest context
+        self.split = not self.auto and (variant == "split" or wl.partition_size is not None)
+        if self.auto:
+            self.max_ctx = wl.max_context_len
+            self.P, need = pf.decode_auto_plan(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                               self.max_ctx, dev)
+            self.ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
         if self.split:
             self.P = wl.partition_size or 512
             self.max_ctx = wl.max_context_len
             self.ws = pf.alloc_workspace(wl.num_seqs, wl.num_q_heads, wl.head_dim, self.max_ctx, self.P, dev)
         self.fused = self.append and not self.split and variant == "fused"
-        self.kernels_per_step = 1 if self.fused else (1 if self.append else 0) + (2 if self.split else 1)
+        self.kernels_per_step = 1 if self.fused else (1 if self.append else 0) + (
+            2 if self.split or (self.auto and self.P) else 1)
         self.dominant = "partition" if self.split else ("decode_append" if self.fused else "decode")
 
     def step(self, ev=None):
@@ -208,6 +215,12 @@ class Runner:
             pf.reshape_and_cache(self.nk, self.nv, self.sm, self.kc, self.vc)
         if ev is not None:
             ev[0].record()
+        if self.auto:    # the whole call (single pass, or partition + merge) is the dominant region
+            pf.paged_attention_decode_auto(self.q, self.kc, self.vc, self.bt, self.cl, self.max_ctx, self.wl.scale,
+                                           self.ws, self.out)
+            if ev is not None:
+                ev[1].record()
+            return
         if self.split:
             pf.paged_attention_decode_partition(self.q, self.kc, self.vc, self.bt, self.cl, self.P, self.max_ctx,
                                                 self.ws, self.wl.scale)
@@ -534,7 +547,8 @@ def main():
             del mr
         del runner
         torch.cuda.empty_cache()
-        for idx, variant in [(1, "decode"), (2, "decode"), (3, "decode"), (3, "fused"), (5, "decode")]:
+        for idx, variant in [(1, "decode"), (2, "decode"), (2, "auto"), (3, "decode"), (3, "fused"), (5, "decode"),
+                             (5, "auto")]:
             if idx == args.workload and variant == "decode":
                 continue
             w = make_config(idx)
@@ -545,9 +559,11 @@ def main():
             ms_s, ms_d, _ = time_steps(r, n, 10, fl)
             pf.check_device_error()
             b = r.step_bytes()
-            extras[CONFIGS[idx].name + ("_fused" if r.fused else "")] = {
+            extras[CONFIGS[idx].name + ("_fused" if r.fused else "_auto" if r.auto else "")] = {
                 "description": CONFIGS[idx].description,
                 "step": "append and decode fused in one launch" if r.fused else
+                        (f"decode_auto ({'partition + merge, P=' + str(r.P) if r.P else 'single pass'}, "
+                         f"max_context_len {r.max_ctx})") if r.auto else
                         ("append + " if r.append else "") + ("partition + merge" if r.split else "decode"),
                 "us_per_step": round(ms_s * 1e3, 2) if fl is None else None,
                 "us_dominant_kernel": round(ms_d * 1e3, 2),
