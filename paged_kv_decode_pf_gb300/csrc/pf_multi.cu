@@ -51,7 +51,40 @@ struct MultiParams {
     float scale_log2;
     int num_seqs, q_len, num_q_heads, num_kv_heads, group, rows;
     int block_size, block_shift, max_blocks_per_seq;
+    int sorted;  // CTA b serves the sequence of rank b / Hkv, longest first (num_seqs <= kMultiSortMax)
 };
+
+constexpr int kMultiSortMax = 512;
+
+// The sequence of rank r when the sequences are ordered longest first (ties by index):
+// every CTA ranks the lengths in shared memory, so the hardware's in-order dispatch of
+// the grid starts the longest items first and they do not form the launch's tail.
+template <int NT>
+__device__ __forceinline__ int multi_sorted_seq(const MultiParams& p, int r) {
+    __shared__ __align__(16) int keys[kMultiSortMax];
+    __shared__ int s_seq;
+    const int S = p.num_seqs, Sp = (S + 3) & ~3;
+    for (int i = threadIdx.x; i < Sp; i += NT) {
+        int key = -1;
+        if (i < S) {
+            const int Li = min(max(__ldg(p.context_lens + i), 0), (1 << 20) - 1);
+            key = (Li << 10) | (1023 - i);
+        }
+        keys[i] = key;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < S; i += NT) {
+        const int ki = keys[i];
+        int rank = 0;
+        for (int j = 0; j < Sp; j += 4) {
+            const int4 kj = *reinterpret_cast<const int4*>(keys + j);
+            rank += int(kj.x > ki) + int(kj.y > ki) + int(kj.z > ki) + int(kj.w > ki);
+        }
+        if (rank == r) s_seq = i;
+    }
+    __syncthreads();
+    return s_seq;
+}
 
 template <int D, int NW, int NST>
 struct MultiLayout {
@@ -90,7 +123,8 @@ __global__ void __launch_bounds__(NW * 32) paged_multi_query_kernel(const __grid
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int Hkv = p.num_kv_heads, G = p.group, Q = p.q_len, RR = p.rows, Hq = p.num_q_heads;
-    const int seq = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
+    const int kvh = blockIdx.x % Hkv;
+    const int seq = p.sorted ? multi_sorted_seq<NW * 32>(p, blockIdx.x / Hkv) : blockIdx.x / Hkv;
     const int L = __ldg(p.context_lens + seq);
     const bool len_bad = L < 0 || (long long)L > (long long)p.max_blocks_per_seq * p.block_size;
     auto out_row = [&](int r) -> float* {  // query row r = j * G + h
@@ -422,7 +456,8 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32, 2) paged_multi_query_wide_
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hkv = p.num_kv_heads, G = p.group, Q = p.q_len, RR = p.rows, Hq = p.num_q_heads;
-    const int seq = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
+    const int kvh = blockIdx.x % Hkv;
+    const int seq = p.sorted ? multi_sorted_seq<(MT * NG + 1) * 32>(p, blockIdx.x / Hkv) : blockIdx.x / Hkv;
     const int L = __ldg(p.context_lens + seq);
     const bool len_bad = L < 0 || (long long)L > (long long)p.max_blocks_per_seq * p.block_size;
     auto out_row = [&](int r) -> float* {  // query row r = j * G + h
@@ -892,6 +927,7 @@ extern "C" pf_status pf_paged_attention_multi_query(const void* q, const void* k
     p.block_size = block_size;
     p.block_shift = (block_size & (block_size - 1)) == 0 ? __builtin_ctz(unsigned(block_size)) : -1;
     p.max_blocks_per_seq = max_blocks_per_seq;
+    p.sorted = num_seqs > 1 && num_seqs <= kMultiSortMax;
     const cudaError_t e = head_dim == 64 ? launch_multi_any<64>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream))
                                          : launch_multi_any<128>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;

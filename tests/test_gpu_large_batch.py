@@ -42,3 +42,19 @@ def test_split_above_1024_sequences(pf, oracle_lib):
     ref = oracle_lib.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
     check_close(got, ref)
     assert not got[wl.context_lens == 0].any()
+
+
+@pytest.mark.parametrize("q_len", [2, 8])
+def test_multi_query_above_512_sequences(pf, oracle_lib, q_len):
+    """Past 512 sequences the multi-token kernels (16-row and wide) take natural order."""
+    import torch
+    from workloads import multi_query
+    wl = make_workload("bigmq", 600, 16, 4, 64, 16, ("uniform", 1, 90), seed=84 + q_len)
+    q = multi_query(wl, q_len)
+    d = to_device(wl)
+    qt = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).view(torch.bfloat16).cuda()
+    got = pf.paged_attention_multi_query(qt, d["k_cache"], d["v_cache"], d["block_tables"],
+                                         d["context_lens"]).cpu().numpy()
+    assert pf.get_device_error() == pf.PF_OK
+    ref = oracle_lib.paged_attention_multi(q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    check_close(got, ref)
