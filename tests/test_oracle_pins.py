@@ -379,6 +379,20 @@ def test_multi_query_rows_are_decodes_of_their_prefix(oracle_lib):
         assert np.array_equal(m[:, j], ref)
 
 
+def test_multi_query_long_draft_rows_are_decodes_of_their_prefix(oracle_lib):
+    """The same property with 16 new tokens at g = 4 (64 query rows per kv head, the widest the
+    GPU kernels take) and a sequence shorter than the draft (its first rows are zero)."""
+    wl = small(S=3, Hq=8, Hkv=2, lengths=(12, 70, 129), seed=22)
+    Q = 16
+    q = _multi(wl, Q)
+    m = oracle_lib.paged_attention_multi(q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    for j in range(Q):
+        lens = np.maximum(wl.context_lens - Q + j + 1, 0).astype(np.int32)
+        ref = oracle_lib.paged_attention(q[:, j], wl.k_cache, wl.v_cache, wl.block_tables, lens, wl.scale)
+        assert np.array_equal(m[:, j], ref)
+    assert not m[0, :4].any()
+
+
 def test_multi_query_dense_bruteforce_causal(oracle_lib):
     wl = small(S=2, Hq=4, Hkv=1, D=64, lengths=(7, 20), seed=21)
     Q = 4
