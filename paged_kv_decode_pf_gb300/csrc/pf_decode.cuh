@@ -431,9 +431,9 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     }
     // Decode with append: the new token of this sequence is its position L-1, and its
     // slot must be that position's slot (or -1: nothing to append).  The slot and the
-    // last table entry are loaded here but checked only where they are used -- when the
-    // tile holding position L-1 lands and at the end -- so their latency does not delay
-    // the first copies.  A mismatch writes nothing and NaN-fills the rows.
+    // last table entry are loaded here but checked only after the first copies are
+    // issued, so their latency does not delay them.  A mismatch writes nothing and
+    // NaN-fills the rows.
     long long app_slot = -1;
     int app_blk = -1;
     if constexpr (APPEND) {
@@ -528,6 +528,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     wa.init(lane);
     wa.load_q(p.q + (size_t(seq) * Hq + qh0) * D);
     wa.reset();
+    // decode with append: the new token's cache row, settled once the first copies are in
+    // flight (its inputs were loaded at the start), not re-derived per tile
+    long long app_row = -1;
+    if constexpr (APPEND) app_row = append_row();
 
     bool timed_out = false;
     int k = 0;
@@ -540,8 +544,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         const int nvalid = min(TT, t1 - tile_token(k));
         if constexpr (APPEND) {
             const int r = (L - 1) - tile_token(k);
-            const long long app_row = (r >= 0 && r < TT) ? append_row() : -1;
-            if (app_row >= 0) {
+            if (app_row >= 0 && r >= 0 && r < TT) {
                 // The tile holding the new token: its copy brought the slot's old bytes.
                 // Put the new K/V row in their place, and write it to the cache.
                 constexpr int LB = ROW / 32;  // bytes of the row per lane
@@ -584,7 +587,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         for (int kk = k; kk < last; ++kk) mbar_wait_bounded(bar0 + 8 * (kk % NST), (kk / NST) & 1, p.wait_limit_ns);
     }
     if constexpr (APPEND) {
-        if (append_row() == -2) bad_block = true;  // the slot is not position L-1's: nothing was written
+        if (app_row == -2) bad_block = true;  // the slot is not position L-1's: nothing was written
     }
     if (lane == 0 && bad_block) set_error(p.err, ERR_BOUNDS);
     const bool warp_failed = __any_sync(FULL_MASK, bad_block || timed_out);
