@@ -541,6 +541,7 @@ def main():
                 "step": "multi_query", "us_dominant_kernel": round(ms_d * 1e3, 2), "algorithmic_bytes": mb,
                 "gbs_dominant_kernel": round(mb / (ms_d * 1e-3) / 1e9, 1),
                 "pct_of_8tbs_dominant": round(100 * mb / (ms_d * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
+                "frac_of_measured_peak_dominant": round(mb / (ms_d * 1e-3) / 1e9 / peak, 3),
                 "tflops_dominant_kernel": round(fl / (ms_d * 1e-3) / 1e12, 1),
                 "l2": "inputs larger than L2",
             }
@@ -571,6 +572,7 @@ def main():
                 "gbs_step": round(b / (ms_s * 1e-3) / 1e9, 1) if fl is None else None,
                 "gbs_dominant_kernel": round(r.dominant_bytes() / (ms_d * 1e-3) / 1e9, 1),
                 "pct_of_8tbs_dominant": round(100 * r.dominant_bytes() / (ms_d * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
+                "frac_of_measured_peak_dominant": round(r.dominant_bytes() / (ms_d * 1e-3) / 1e9 / peak, 3),
                 "seq_steps_per_s": round(w.num_seqs / ((ms_s if fl is None else ms_d) * 1e-3), 1),
                 "l2": "flushed between steps (kernel time only)" if fl is not None else "inputs larger than L2",
             }
