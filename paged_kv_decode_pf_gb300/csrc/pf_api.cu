@@ -96,6 +96,9 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __r
 // weight sum over all partitions itself (lane-parallel), so no barrier is needed
 // before the accumulation.  WPR grows with the partition count (host side).
 constexpr int MERGE_WARPS = 8;
+#ifndef PF_MERGE_WPR16_FROM
+#define PF_MERGE_WPR16_FROM 256  // partitions per row from which a row takes 16 warps
+#endif
 
 // Loads of the partials the partition pass wrote just before: each is read once.
 __device__ __forceinline__ float ld_stream(const float* p) {
@@ -118,8 +121,12 @@ __device__ __forceinline__ void ld_stream_row(const float* src, bool in, float (
     }
 }
 
+// warps of a merge CTA: MERGE_WARPS, or WPR when one row takes more
+template <int WPR>
+constexpr int merge_warps() { return WPR > MERGE_WARPS ? WPR : MERGE_WARPS; }
+
 template <int D, int WPR>
-__global__ void __launch_bounds__(MERGE_WARPS * 32) lse_merge_kernel(const float* __restrict__ tmp_out,
+__global__ void __launch_bounds__(merge_warps<WPR>() * 32) lse_merge_kernel(const float* __restrict__ tmp_out,
                                                                      const float* __restrict__ tmp_m,
                                                                      const float* __restrict__ tmp_l,
                                                                      const int32_t* __restrict__ context_lens,
@@ -128,9 +135,10 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) lse_merge_kernel(const float
                                                                      int max_context_len, float* __restrict__ out,
                                                                      unsigned* err) {
     constexpr int DPL = D / 32;
-    constexpr int ROWS = MERGE_WARPS / WPR;
+    constexpr int NWM = merge_warps<WPR>();
+    constexpr int ROWS = NWM / WPR;
     constexpr float kLog2e = 1.4426950408889634f;
-    __shared__ __align__(16) float accs[MERGE_WARPS][D];
+    __shared__ __align__(16) float accs[NWM][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rloc = warp / WPR, sub = warp % WPR;
     const long long row = (long long)blockIdx.x * ROWS + rloc;   // (seq, q head)
@@ -215,7 +223,7 @@ static cudaError_t launch_merge_wpr(unsigned blocks, cudaStream_t s, const float
                                     int partition_size, int np, int max_context_len, float* out, unsigned* err) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks);
-    cfg.blockDim = dim3(MERGE_WARPS * 32);
+    cfg.blockDim = dim3(merge_warps<WPR>() * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -238,6 +246,8 @@ static cudaError_t launch_merge(int wpr, unsigned blocks, cudaStream_t s, const 
                                               partition_size, np, max_context_len, out, err);
         case 4: return launch_merge_wpr<D, 4>(blocks, s, to, tm, tl, context_lens, num_seqs, num_q_heads,
                                               partition_size, np, max_context_len, out, err);
+        case 16: return launch_merge_wpr<D, 16>(blocks, s, to, tm, tl, context_lens, num_seqs, num_q_heads,
+                                                 partition_size, np, max_context_len, out, err);
         default: return launch_merge_wpr<D, 8>(blocks, s, to, tm, tl, context_lens, num_seqs, num_q_heads,
                                                partition_size, np, max_context_len, out, err);
     }
@@ -504,8 +514,9 @@ pf_status pf_paged_attention_merge(const void* workspace, const int32_t* context
     const char* ws = static_cast<const char*>(workspace);
     const long long rows = (long long)num_seqs * num_q_heads;
     // warps per row: enough that each warp has about 16 partitions or fewer to add
-    const int wpr = np >= 128 ? 8 : np >= 64 ? 4 : np >= 32 ? 2 : 1;
-    const long long blocks = (rows + (MERGE_WARPS / wpr) - 1) / (MERGE_WARPS / wpr);
+    const int wpr = np >= PF_MERGE_WPR16_FROM ? 16 : np >= 128 ? 8 : np >= 64 ? 4 : np >= 32 ? 2 : 1;
+    const int rows_per_cta = (wpr > MERGE_WARPS ? wpr : MERGE_WARPS) / wpr;
+    const long long blocks = (rows + rows_per_cta - 1) / rows_per_cta;
     if (blocks > INT32_MAX) return PF_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float* to = reinterpret_cast<const float*>(ws + off_o);
