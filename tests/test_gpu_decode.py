@@ -45,19 +45,12 @@ def test_cont_batch_append_then_decode(pf, oracle_lib, config_workload):
     check_close(got, oracle_out(oracle_lib, wl, kc, vc))
 
 
-def test_llama3_8b_full_size_sampled(pf, oracle_lib, config_workload):
-    """256 sequences, 4.8 GB of KV, the launch the bench times; 48 sampled (seq, head) rows
-    plus every head of the longest sequence are checked against the oracle."""
+def test_llama3_8b_full_size(pf, oracle_lib, config_workload):
+    """256 sequences, 4.8 GB of KV, the launch the bench times: every output row against the
+    oracle (about a second of the host's cores)."""
     wl = config_workload(4)
     got = decode(pf, to_device(wl))
-    assert np.all(np.isfinite(got))
-    rng = np.random.default_rng(123)
-    pairs = [(int(rng.integers(wl.num_seqs)), int(rng.integers(wl.num_q_heads))) for _ in range(48)]
-    longest = int(np.argmax(wl.context_lens))
-    pairs += [(longest, h) for h in range(wl.num_q_heads)]
-    ref = oracle_lib.paged_attention_pairs(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
-                                           wl.scale, pairs)
-    check_close(np.stack([got[i, h] for i, h in pairs]), ref)
+    check_close(got, oracle_out(oracle_lib, wl))
     torch.cuda.empty_cache()
 
 
@@ -65,10 +58,7 @@ def test_long_context_single_pass(pf, oracle_lib, config_workload):
     """The 131072-token sequence through the single-pass kernel (one CTA per kv head)."""
     wl = config_workload(5)
     got = decode(pf, to_device(wl))
-    pairs = [(0, h) for h in range(0, wl.num_q_heads, 3)] + [(1, 0), (2, 5), (3, 31)]
-    ref = oracle_lib.paged_attention_pairs(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
-                                           wl.scale, pairs)
-    check_close(np.stack([got[i, h] for i, h in pairs]), ref)
+    check_close(got, oracle_out(oracle_lib, wl))
 
 
 EDGE_LENGTHS = [1, 15, 16, 17, 31, 32, 33, 511, 512, 513]
