@@ -85,3 +85,15 @@ def test_multi_query_rows_beyond_sixty_four_are_unsupported(pf):
     with pytest.raises(pf.PFError) as e:
         pf.paged_attention_multi_query(q, d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"])
     assert e.value.status == pf.PF_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("q_len", [4, 16])
+def test_multi_query_llama3_full_size(pf, oracle_lib, config_workload, q_len):
+    """The launches the bench times: all 256 Llama-3-shaped sequences (4.8 GB of K/V) with 4
+    and with 16 draft tokens (16 and 64 query rows per kv head), every row against the oracle."""
+    wl = config_workload(4)
+    q = multi_query(wl, q_len)
+    got = run_multi(pf, to_device(wl), q)
+    ref = oracle_lib.paged_attention_multi(q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    check_close(got, ref)
+    torch.cuda.empty_cache()
