@@ -321,10 +321,10 @@ class MultiQueryRunner:
     """pf_paged_attention_multi_query over a resident workload: the last q_len tokens of
     every sequence are its new tokens (draft tokens under verification)."""
 
-    def __init__(self, pf, runner, q_len):
+    def __init__(self, pf, runner, q_len, kernel="mma"):
         import torch
         from workloads import multi_query
-        self.pf, self.r, self.q_len = pf, runner, q_len
+        self.pf, self.r, self.q_len, self.kernel = pf, runner, q_len, kernel
         wl = runner.wl
         q = multi_query(wl, q_len)
         self.q = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).view(torch.bfloat16).to(runner.dev)
@@ -335,7 +335,7 @@ class MultiQueryRunner:
         r = self.r
         if ev is not None:
             ev[0].record()
-        self.pf.paged_attention_multi_query(self.q, r.kc, r.vc, r.bt, r.cl, r.wl.scale, self.out)
+        self.pf.paged_attention_multi_query(self.q, r.kc, r.vc, r.bt, r.cl, r.wl.scale, self.out, kernel=self.kernel)
         if ev is not None:
             ev[1].record()
 
@@ -526,17 +526,21 @@ def main():
     extras = {}
     if not args.no_extras and rank == 0:
         g = wl.num_q_heads // wl.num_kv_heads
-        for q_len in (4, 8, 12, 16):
+        runs = [(q_len, "mma") for q_len in (4, 8, 12, 16)]
+        if wl.head_dim == 128:
+            runs += [(8, "tcgen05"), (16, "tcgen05")]
+        for q_len, kernel in runs:
             if runner.split or g * q_len > 64:
                 continue
             # the same resident cache, with the last q_len tokens of every sequence as new (draft) tokens
-            mr = MultiQueryRunner(pf, runner, q_len)
+            mr = MultiQueryRunner(pf, runner, q_len, kernel)
             ms_s, ms_d, _ = time_steps(mr, 200, 10)
             pf.check_device_error()
             mb = mr.step_bytes()
             fl = mr.step_flops()
-            extras[CONFIGS[args.workload].name + f"_multi_query_q{q_len}"] = {
-                "description": f"pf_paged_attention_multi_query on the same cache: {q_len} new tokens per "
+            name = "pf_paged_attention_multi_query" + ("_tcgen05" if kernel == "tcgen05" else "")
+            extras[CONFIGS[args.workload].name + f"_multi_query_q{q_len}" + ("_tcgen05" if kernel == "tcgen05" else "")] = {
+                "description": f"{name} on the same cache: {q_len} new tokens per "
                                f"sequence, causal among them ({g * q_len} query rows per kv head)",
                 "step": "multi_query", "us_dominant_kernel": round(ms_d * 1e3, 2), "algorithmic_bytes": mb,
                 "gbs_dominant_kernel": round(mb / (ms_d * 1e-3) / 1e9, 1),

@@ -176,11 +176,15 @@ PF_API pf_status pf_paged_attention_decode_append(const void* q, const void* k_n
  *
  *   out[i][j][h][:] = sum_{t <= L_i - q_len + j} softmax_t(scale * q[i][j][h] . K_t) V_t
  *
- * A row whose position is negative (L_i < q_len) is zero.  The scores and P.V
+ * A row whose position is negative (L_i < q_len) is zero.  A NaN or infinite
+ * key at a position a row cannot see leaves that row alone (its score is
+ * replaced); a NaN or infinite *value* there may make the row NaN, since the
+ * tensor-core P.V product multiplies it by the row's zero probability.  Finite
+ * caches are unaffected.  The scores and P.V
  * run on tensor cores (mma.sync, bf16 inputs, fp32 accumulation; the
  * probabilities enter P.V as a bf16 high part plus a bf16 remainder).  Up to 16
  * rows per kv head (g * q_len) one CTA's four warps split the tokens; from 17 to
- * 64 rows each 16-row tile has its own warp and a producer warp streams K/V to
+ * 64 rows each 16-row tile has its own warp and one or two producer warps stream K/V to
  * all of them.
  *
  *   q    [num_seqs, q_len, num_q_heads, head_dim] bf16, 16-byte aligned
@@ -194,6 +198,30 @@ PF_API pf_status pf_paged_attention_multi_query(const void* q, const void* k_cac
                                                 int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
                                                 int head_dim, int block_size, int max_blocks_per_seq,
                                                 int64_t num_blocks, float scale, float* out, pf_stream_t stream);
+
+/*
+ * The same operation as pf_paged_attention_multi_query, with both products on
+ * the fifth-generation tensor cores (tcgen05.mma, accumulators in tensor
+ * memory): per (sequence, kv head) one CTA streams K/V tiles of 64 tokens; the
+ * scores S = Q K^T (query rows from tensor memory) and O = P V (probabilities,
+ * as bf16 high part plus remainder, from tensor memory) are single-CTA MMAs
+ * whose operands the TMA copies straight from the cache blocks.  Results agree
+ * with pf_paged_attention_multi_query to fp32 rounding.  On the Llama-3-8B-
+ * shaped batch it is slower than that kernel at every row count (its K/V
+ * stages are held through the whole score, softmax and P.V chain, and four
+ * copy-issuing warps keep fewer bytes in flight than the mma.sync kernel's two
+ * CTAs per SM); it is the tensor-memory formulation of the step, kept as an
+ * alternative.
+ *
+ * Supported: head_dim == 128 (else PF_ERR_UNSUPPORTED); the other shapes,
+ * arguments and errors as pf_paged_attention_multi_query.
+ */
+PF_API pf_status pf_paged_attention_multi_query_tcgen05(const void* q, const void* k_cache, const void* v_cache,
+                                                        const int32_t* block_tables, const int32_t* context_lens,
+                                                        int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                                        int head_dim, int block_size, int max_blocks_per_seq,
+                                                        int64_t num_blocks, float scale, float* out,
+                                                        pf_stream_t stream);
 
 /*
  * Split over context partitions ("flash-decoding") for long contexts.

@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.pf_paged_attention_multi_query.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i64, f32, P,
                                                      P]
         L.pf_paged_attention_multi_query.restype = st
+        L.pf_paged_attention_multi_query_tcgen05.argtypes = L.pf_paged_attention_multi_query.argtypes
+        L.pf_paged_attention_multi_query_tcgen05.restype = st
         _LIB = L
     return _LIB
 
@@ -207,9 +209,13 @@ def paged_attention_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: t
 
 def paged_attention_multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                                 block_tables: torch.Tensor, context_lens: torch.Tensor,
-                                scale: Optional[float] = None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                                scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                                kernel: str = "mma") -> torch.Tensor:
     """q [S, q_len, Hq, D]: the last q_len tokens of each sequence, already in the cache, attend causally.
-    Returns out [S, q_len, Hq, D] fp32.  Needs (Hq / Hkv) * q_len <= 64."""
+    Returns out [S, q_len, Hq, D] fp32.  Needs (Hq / Hkv) * q_len <= 64.  kernel="tcgen05" runs
+    pf_paged_attention_multi_query_tcgen05 (D = 128 only) instead of pf_paged_attention_multi_query."""
+    if kernel not in ("mma", "tcgen05"):
+        raise ValueError(f"paged_attention_multi_query: unknown kernel {kernel!r}")
     _cuda(q, "q", _BF16, 4)
     _cuda(k_cache, "k_cache", _BF16, 4)
     _cuda(v_cache, "v_cache", _BF16, 4)
@@ -225,10 +231,10 @@ def paged_attention_multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
     _cuda(out, "out", (torch.float32,), 4)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     with torch.cuda.device(q.device):
-        _check(lib().pf_paged_attention_multi_query(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                                                    block_tables.data_ptr(), context_lens.data_ptr(), S, Q, Hq, Hkv,
-                                                    D, bs, MB, NB, scale, out.data_ptr(), _stream(q.device)),
-               "pf_paged_attention_multi_query")
+        name = "pf_paged_attention_multi_query" + ("_tcgen05" if kernel == "tcgen05" else "")
+        _check(getattr(lib(), name)(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+                                    context_lens.data_ptr(), S, Q, Hq, Hkv, D, bs, MB, NB, scale, out.data_ptr(),
+                                    _stream(q.device)), name)
     return out
 
 

@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(NW * 32) paged_multi_query_kernel(const __grid
 // g = 4, or a 64-token prompt chunk of a multi-head model).  One CTA per
 // (sequence, kv head) with MT x NG consumer warps -- warp w owns query rows
 // [16 mt, 16 mt + 16), mt = w % MT, as one m16 tile, and takes the stages
-// k = grp, grp + NG, ... of its group grp = w / MT -- and one producer warp.  With
+// k = grp, grp + NG, ... of its group grp = w / MT -- and two producer warps.  With
 // 32 rows or fewer two groups split the stages (four consumer warps, like the
 // 16-row kernel's token split) and merge their (m, l, O) at the end.  The producer's lane 0
 // streams the sequence in stages of 64 tokens (four 16-token tiles, K and V, by TMA
@@ -408,8 +408,8 @@ constexpr int kWideMaxRows = 64;
 #ifndef PF_WIDE_OPT_4
 #define PF_WIDE_OPT_4 3
 #endif
-constexpr int kWideSub = 4;     // 16-token tiles per stage
-constexpr int kWideStages = 3;
+constexpr int kWideSub = 4;      // 16-token tiles per stage
+constexpr int kWideMaxProd = 2;  // producer warps at most (kWideSub / NPW tiles of each stage apiece)
 
 template <int D, int NST, int NC = 0>
 struct WideLayout {
@@ -421,11 +421,11 @@ struct WideLayout {
     static constexpr int STAGE = 2 * KV;
     static constexpr size_t FULL = size_t(NST) * STAGE;     // NST mbarriers
     static constexpr size_t EMPTY = FULL + size_t(NST) * 8;  // NST mbarriers
-    static constexpr size_t BAD = EMPTY + size_t(NST) * 8;   // NST ints: bit u = tile u had no copy
+    static constexpr size_t BAD = EMPTY + size_t(NST) * 8;   // [NST][producer] ints: bit u = tile u had no copy
     // query rows in shared memory (when the registers are short): per consumer warp 16 rows
     // of D bf16, rows padded by 16 bytes so the ldmatrix reads are free of bank conflicts
     static constexpr int QSTRIDE = D * 2 + 16;
-    static constexpr size_t QAREA = BAD + ((NST * 4 + 15) / 16) * 16;
+    static constexpr size_t QAREA = BAD + ((NST * 4 * kWideMaxProd + 15) / 16) * 16;
     static constexpr size_t BYTES = QAREA + size_t(NC) * 16 * QSTRIDE;
     static constexpr size_t ALLOC = BYTES + 1024;           // room to align to 1024
 };
@@ -434,8 +434,8 @@ struct WideLayout {
 // step), kWideSplit (two score accumulator chains)
 constexpr int kWideQs = 1, kWidePairs = 2, kWideSplit = 4;
 
-template <int D, int MT, int NG, int NST, int OPT>
-__global__ void __launch_bounds__((MT * NG + 1) * 32, 2) paged_multi_query_wide_kernel(
+template <int D, int MT, int NG, int NST, int OPT, int NPW>
+__global__ void __launch_bounds__((MT * NG + NPW) * 32, 2) paged_multi_query_wide_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v, const MultiParams p) {
     constexpr bool QS = (OPT & kWideQs) != 0;
     using Lay = WideLayout<D, NST, QS ? MT * NG : 0>;
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32, 2) paged_multi_query_wide_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hkv = p.num_kv_heads, G = p.group, Q = p.q_len, RR = p.rows, Hq = p.num_q_heads;
     const int kvh = blockIdx.x % Hkv;
-    const int seq = p.sorted ? multi_sorted_seq<(MT * NG + 1) * 32>(p, blockIdx.x / Hkv) : blockIdx.x / Hkv;
+    const int seq = p.sorted ? multi_sorted_seq<(MT * NG + NPW) * 32>(p, blockIdx.x / Hkv) : blockIdx.x / Hkv;
     const int L = __ldg(p.context_lens + seq);
     const bool len_bad = L < 0 || (long long)L > (long long)p.max_blocks_per_seq * p.block_size;
     auto out_row = [&](int r) -> float* {  // query row r = j * G + h
@@ -466,70 +466,136 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32, 2) paged_multi_query_wide_
     };
     if (len_bad) {
         if (threadIdx.x == 0) set_error(p.err, ERR_BOUNDS);
-        for (int e = threadIdx.x; e < RR * D; e += (NC + 1) * 32) out_row(e / D)[e % D] = NAN;
+        for (int e = threadIdx.x; e < RR * D; e += (NC + NPW) * 32) out_row(e / D)[e % D] = NAN;
         return;
     }
     const int nstages = (L + SUBTOK - 1) / SUBTOK;
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < NST; ++s) {
-            mbar_init(full0 + 8 * s, 1);
+            mbar_init(full0 + 8 * s, NPW);
             mbar_init(empty0 + 8 * s, MT);
         }
         mbar_init_fence();
     }
     __syncthreads();
 
-    if (warp == NC) {
-        // ---- producer: lane 0 fills stage k % NST once its consumers have released it
-        if (lane != 0) return;
-        const int32_t* trow = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
-        const int bs = p.block_size, bshift = p.block_shift;
-        auto block_index = [&](int tok) { return bshift >= 0 ? (tok >> bshift) : (tok / bs); };
-        auto block_offset = [&](int tok) { return bshift >= 0 ? (tok & (bs - 1)) : (tok % bs); };
-        const uint64_t policy = l2_policy_evict_first();
-        int cur[kWideSub], nxt[kWideSub];
-        auto entries = [&](int k, int (&e)[kWideSub]) {  // table entries of stage k's tiles
+    if (NPW == 1 ? warp == NC : warp >= NC) {
+        if constexpr (NPW == 1) {
+            // ---- producer: lane 0 fills stage k % NST once its consumers have released it
+            if (lane != 0) return;  // one producer: lane 0 alone
+            const int32_t* trow = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
+            const int bs = p.block_size, bshift = p.block_shift;
+            auto block_index = [&](int tok) { return bshift >= 0 ? (tok >> bshift) : (tok / bs); };
+            auto block_offset = [&](int tok) { return bshift >= 0 ? (tok & (bs - 1)) : (tok % bs); };
+            const uint64_t policy = l2_policy_evict_first();
+            int cur[kWideSub], nxt[kWideSub];
+            auto entries = [&](int k, int (&e)[kWideSub]) {  // table entries of stage k's tiles
 #pragma unroll
-            for (int u = 0; u < kWideSub; ++u) {
-                const int tok = k * SUBTOK + u * TT;
-                e[u] = tok < L ? __ldg(trow + block_index(tok)) : 0;
+                for (int u = 0; u < kWideSub; ++u) {
+                    const int tok = k * SUBTOK + u * TT;
+                    e[u] = tok < L ? __ldg(trow + block_index(tok)) : 0;
+                }
+            };
+            if (nstages > 0) entries(0, cur);
+            for (int k = 0; k < nstages; ++k) {
+                if (k + 1 < nstages) entries(k + 1, nxt);  // a stage ahead
+                const int s = k % NST;
+                if (k >= NST && !mbar_wait_bounded(empty0 + 8 * s, ((k / NST) - 1) & 1, p.wait_limit_ns)) {
+                    set_error(p.err, ERR_TIMEOUT);  // the consumers' own waits give up in turn
+                    return;
+                }
+                uint32_t bytes = 0;
+                int badmask = 0;
+#pragma unroll
+                for (int u = 0; u < kWideSub; ++u) {
+                    if (k * SUBTOK + u * TT >= L) continue;
+                    if (cur[u] >= 0 && (long long)cur[u] < p.num_blocks) bytes += 2 * SUBTILE;
+                    else badmask |= 1 << u;
+                }
+                bad[s] = badmask;
+                if (badmask) set_error(p.err, ERR_BOUNDS);
+                const uint32_t full = full0 + 8 * s;
+                const uint32_t dst = smem_u32(smem) + uint32_t(s) * STAGE;
+                mbar_arrive_expect_tx(full, bytes);
+#pragma unroll
+                for (int u = 0; u < kWideSub; ++u) {
+                    const int tok = k * SUBTOK + u * TT;
+                    if (tok >= L || (badmask >> u) & 1) continue;
+                    const int y = (cur[u] * Hkv + kvh) * bs + block_offset(tok);
+#pragma unroll
+                    for (int hh = 0; hh < HALVES; ++hh) {
+                        tma_load_2d(dst + u * SUBTILE + hh * HALF, &tmap_k, hh * 64, y, full, policy);
+                        tma_load_2d(dst + KV + u * SUBTILE + hh * HALF, &tmap_v, hh * 64, y, full, policy);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kWideSub; ++u) cur[u] = nxt[u];
             }
-        };
-        if (nstages > 0) entries(0, cur);
-        for (int k = 0; k < nstages; ++k) {
-            if (k + 1 < nstages) entries(k + 1, nxt);  // a stage ahead
-            const int s = k % NST;
-            if (k >= NST && !mbar_wait_bounded(empty0 + 8 * s, ((k / NST) - 1) & 1, p.wait_limit_ns)) {
-                set_error(p.err, ERR_TIMEOUT);  // the consumers' own waits give up in turn
-                return;
-            }
-            uint32_t bytes = 0;
-            int badmask = 0;
+        } else {
+            // ---- producer warp pw of NPW: lane 0 fills its kWideSub / NPW tiles of stage k % NST once
+            // the consumers have released it.  The blocks of a sequence lie anywhere in the pool and one
+            // thread's copies to scattered pages are served one after another, so where the registers
+            // allow, two warps issue.
+            // The warp loads the table entries of 32 boxes (8 stages) a batch ahead: lane l holds
+            // box 32 b + l.
+            const int pw = warp - NC;
+            const int32_t* trow = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
+            const int bs = p.block_size, bshift = p.block_shift;
+            auto block_index = [&](int tok) { return bshift >= 0 ? (tok >> bshift) : (tok / bs); };
+            auto block_offset = [&](int tok) { return bshift >= 0 ? (tok & (bs - 1)) : (tok % bs); };
+            auto batch = [&](int b) {
+                const int tok = (32 * b + lane) * TT;
+                return tok < L ? __ldg(trow + block_index(tok)) : 0;
+            };
+            constexpr int SPB = 32 / kWideSub;  // stages per batch
+            const uint64_t policy = l2_policy_evict_first();
+            int ent_cur = batch(0), ent_nxt = batch(1);
+            for (int k = 0; k < nstages; ++k) {
+                if (k > 0 && k % SPB == 0) {
+                    ent_cur = ent_nxt;
+                    ent_nxt = batch(k / SPB + 1);
+                }
+                int e[kWideSub / NPW];
 #pragma unroll
-            for (int u = 0; u < kWideSub; ++u) {
-                if (k * SUBTOK + u * TT >= L) continue;
-                if (cur[u] >= 0 && (long long)cur[u] < p.num_blocks) bytes += 2 * SUBTILE;
-                else badmask |= 1 << u;
-            }
-            bad[s] = badmask;
-            if (badmask) set_error(p.err, ERR_BOUNDS);
-            const uint32_t full = full0 + 8 * s;
-            const uint32_t dst = smem_u32(smem) + uint32_t(s) * STAGE;
-            mbar_arrive_expect_tx(full, bytes);
+                for (int i = 0; i < kWideSub / NPW; ++i)
+                    e[i] = __shfl_sync(FULL_MASK, ent_cur, (k % SPB) * kWideSub + pw * (kWideSub / NPW) + i);
+                const int s = k % NST;
+                bool ok = true;
+                if (lane == 0 && k >= NST) ok = mbar_wait_bounded(empty0 + 8 * s, ((k / NST) - 1) & 1, p.wait_limit_ns);
+                if (!__shfl_sync(FULL_MASK, ok ? 1 : 0, 0)) {
+                    if (lane == 0) set_error(p.err, ERR_TIMEOUT);  // the consumers' own waits give up in turn
+                    return;
+                }
+                if (lane == 0) {
+                    uint32_t bytes = 0;
+                    int badmask = 0;
 #pragma unroll
-            for (int u = 0; u < kWideSub; ++u) {
-                const int tok = k * SUBTOK + u * TT;
-                if (tok >= L || (badmask >> u) & 1) continue;
-                const int y = (cur[u] * Hkv + kvh) * bs + block_offset(tok);
+                    for (int i = 0; i < kWideSub / NPW; ++i) {
+                        const int u = pw * (kWideSub / NPW) + i;
+                        if (k * SUBTOK + u * TT >= L) continue;
+                        if (e[i] >= 0 && (long long)e[i] < p.num_blocks) bytes += 2 * SUBTILE;
+                        else badmask |= 1 << u;
+                    }
+                    bad[NPW * s + pw] = badmask;
+                    if (badmask) set_error(p.err, ERR_BOUNDS);
+                    const uint32_t full = full0 + 8 * s;
+                    const uint32_t dst = smem_u32(smem) + uint32_t(s) * STAGE;
+                    mbar_arrive_expect_tx(full, bytes);
 #pragma unroll
-                for (int hh = 0; hh < HALVES; ++hh) {
-                    tma_load_2d(dst + u * SUBTILE + hh * HALF, &tmap_k, hh * 64, y, full, policy);
-                    tma_load_2d(dst + KV + u * SUBTILE + hh * HALF, &tmap_v, hh * 64, y, full, policy);
+                    for (int i = 0; i < kWideSub / NPW; ++i) {
+                        const int u = pw * (kWideSub / NPW) + i;
+                        const int tok = k * SUBTOK + u * TT;
+                        if (tok >= L || (badmask >> u) & 1) continue;
+                        const int y = (e[i] * Hkv + kvh) * bs + block_offset(tok);
+#pragma unroll
+                        for (int hh = 0; hh < HALVES; ++hh) {
+                            tma_load_2d(dst + u * SUBTILE + hh * HALF, &tmap_k, hh * 64, y, full, policy);
+                            tma_load_2d(dst + KV + u * SUBTILE + hh * HALF, &tmap_v, hh * 64, y, full, policy);
+                        }
+                    }
                 }
             }
-#pragma unroll
-            for (int u = 0; u < kWideSub; ++u) cur[u] = nxt[u];
         }
         return;
     }
@@ -590,9 +656,21 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32, 2) paged_multi_query_wide_
     int k = grp;
     for (; k < nstages; k += NG) {
         const int s = k % NST;
+        if constexpr (NST % NG != 0) {
+            // stage s alternates between the groups, so this group does not wait on every phase of
+            // its full barrier, and a parity names a phase only up to two fills.  Waiting first for
+            // the release of the stage's previous fill (the other group's) pins the barrier to this
+            // fill or the one before it, where the parity is unambiguous.
+            if (k >= NST) {
+                const bool okr = mbar_wait_bounded(empty0 + 8 * s, ((k / NST) - 1) & 1, p.wait_limit_ns);
+                if (__any_sync(FULL_MASK, !okr)) { timed_out = true; break; }
+            }
+        }
         const bool ok = mbar_wait_bounded(full0 + 8 * s, (k / NST) & 1, p.wait_limit_ns);
         if (__any_sync(FULL_MASK, !ok)) { timed_out = true; break; }
-        if (bad[s]) failed = true;  // a tile without its copy: the rows end up NaN
+        int badbits = bad[NPW * s];
+        if constexpr (NPW > 1) badbits |= bad[NPW * s + 1];
+        if (badbits) failed = true;  // a tile without its copy: the rows end up NaN
         unsigned char* Kst = smem + size_t(s) * STAGE;
         unsigned char* Vst = Kst + KV;
         const int tok_base = k * SUBTOK;
@@ -789,6 +867,433 @@ __global__ void __launch_bounds__((MT * NG + 1) * 32, 2) paged_multi_query_wide_
     }
 }
 
+// ---------------------------------------------------------------- tcgen05 variant
+//
+// 17 to 64 query rows per kv head at D = 128, with the scores and the P.V product
+// both on the fifth-generation tensor cores (single-CTA tcgen05.mma, fp32
+// accumulators in tensor memory).  One CTA per (sequence, kv head), thirteen warps,
+// one CTA per SM (by its shared memory), all 512 TMEM columns: the query rows (64
+// columns, bf16 pairs), two score buffers of 64 columns that the probabilities P
+// overwrite in place, and two 128-column buffers for one tile's P.V.
+//  * warps 0-3 stream the sequence in tiles of 64 tokens through a 6-deep ring: warp u
+//    copies the tile's u-th 16-token box of K and of V (TMA tensor copies with the
+//    128-byte swizzle, issued by lane 0) and fetches the block-table entries 32 boxes at
+//    a time, a batch ahead.  The blocks of a sequence lie anywhere in the pool, and one
+//    thread's copies to scattered pages are served one after another, so four issuing
+//    warps are what keeps enough bytes in flight;
+//  * warp 4, lane 0 issues, as soon as each is ready, S(j) = Q K(j)^T -- M = 128 TMEM
+//    lanes (the query rows, each twice), N = 64 tokens, K = D; Q from tensor memory, K
+//    K-major straight from the swizzled stage -- and O(j) = P(j) V(j) -- M = 128, N = D,
+//    K = 64 tokens; P from tensor memory, V MN-major from the stage -- twice, for P's
+//    bf16 hi and lo parts;
+//  * warps 5-12, two per TMEM lane quarter (a warp may only read its quarter).  Query
+//    row r sits in lanes 32 (r % 4) + r / 4 and 16 above it, so every quarter holds 16
+//    rows twice and the work is spread over the four SM sub-partitions.  For a tile, the
+//    four threads that see row r (a lane pair in each of the quarter's two warps) each
+//    take 16 of the 64 scores, combine their maxima, run the fp32 online softmax and
+//    write the pair's 32 probabilities, as bf16 hi and lo parts, over the scores they
+//    read.  For the tile's O they each add 32 of the row's 128 dimensions into registers,
+//    rescaled by the row's factor, which every one of them holds, and write those
+//    outputs at the end.
+// The scores of one tile and the P.V product of the previous one run on the tensor
+// cores while the softmax runs on the CUDA cores.  Every wait is bounded; one that
+// gives up raises an abort flag that ends the others at once, and every role still
+// runs all its iterations, so the CTA stays in step and releases its tensor memory.
+constexpr int kTcTok = 64;        // tokens per tile
+constexpr int kTcStages = 6;      // K/V ring depth
+constexpr int kTcRows = 64;       // query rows per kv head
+constexpr int kTcCols = 512;      // TMEM columns
+constexpr int kTcProducers = 4;   // issuing warps, one per 16-token box of a tile
+constexpr int kTcThreads = 32 * (kTcProducers + 1 + 8);
+
+struct TcLayout {
+    static constexpr int KVHALF = kTcTok * 128;       // 64 tokens x 64 dims of bf16
+    static constexpr int STAGE = 4 * KVHALF;          // K dims [0,64), [64,128); V the same
+    static constexpr int STAGES = 0;
+    static constexpr int NBARS = 2 * kTcStages + 10;
+    static constexpr int BARS = STAGES + kTcStages * STAGE;
+    static constexpr int PMAX = BARS + ((NBARS * 8 + 15) / 16) * 16;  // [2 halves][128 lanes] partial maxima
+    static constexpr int LSUM = PMAX + 2 * 128 * 4;                   // [2 halves][64] partial row sums
+    static constexpr int MISC = LSUM + 2 * kTcRows * 4;               // TMEM base, bad-block flag, abort flag
+    static constexpr int BYTES = MISC + 16;
+    static constexpr int ALLOC = BYTES + 1024;                        // room to align to 1024
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
+    const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v, const MultiParams p) {
+    constexpr int D = 128, NT = kTcThreads, TOK = kTcTok, ST = kTcStages, NR = kTcRows;
+    constexpr int SUB = TOK / kTileTokens;  // 16-token boxes per tile
+    constexpr int NMW = 8;                  // math warps
+    constexpr int NP = kTcProducers, MMAW = kTcProducers;  // producer warps 0 .. NP-1, then the MMA warp
+    static_assert(NP == SUB, "one producer warp per box of a tile");
+    // TMEM columns: query rows, score / probability buffer b, P.V buffer b
+    constexpr uint32_t TQ = 0;
+    auto TS = [](int b) { return uint32_t(64 + 64 * b); };
+    auto TO = [](int b) { return uint32_t(256 + 128 * b); };
+    using Lay = TcLayout;
+    // mbarriers: K/V ring full / empty, scores ready, probabilities ready, P.V ready, P.V
+    // read, query rows stored, all MMAs done
+    enum { FULL = 0, EMPTY = ST, SFULL = 2 * ST, PFULL = SFULL + 2, OFULL = PFULL + 2, OFREE = OFULL + 2,
+           QREADY = OFREE + 2, DONE = QREADY + 1 };
+    static_assert(DONE + 1 == Lay::NBARS, "barrier count");
+
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // swizzled operands need 1 KiB alignment
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + uint32_t(Lay::BARS + 8 * i); };
+    float* pmax = reinterpret_cast<float*>(smem + Lay::PMAX);
+    float* lsum = reinterpret_cast<float*>(smem + Lay::LSUM);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
+    volatile int* bad = reinterpret_cast<volatile int*>(smem + Lay::MISC + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::MISC + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Hkv = p.num_kv_heads, G = p.group, Q = p.q_len, RR = p.rows, Hq = p.num_q_heads;
+    const int kvh = blockIdx.x % Hkv;
+    const int seq = p.sorted ? multi_sorted_seq<NT>(p, blockIdx.x / Hkv) : blockIdx.x / Hkv;
+    const int L = __ldg(p.context_lens + seq);
+    const bool len_bad = L < 0 || (long long)L > (long long)p.max_blocks_per_seq * p.block_size;
+    auto out_row = [&](int r) -> float* {  // query row r = j * G + h
+        const int j = r / G, h = r - (r / G) * G;
+        return p.out + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D;
+    };
+    if (len_bad) {
+        if (threadIdx.x == 0) set_error(p.err, ERR_BOUNDS);
+        for (int e = threadIdx.x; e < RR * D; e += NT) out_row(e / D)[e % D] = NAN;
+        return;
+    }
+    const int nt = (L + TOK - 1) / TOK;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Lay::NBARS; ++i) {
+            const bool by_warps = i == PFULL || i == PFULL + 1 || i == OFREE || i == OFREE + 1 || i == QREADY;
+            mbar_init(bar(i), by_warps ? NMW : (i < FULL + ST ? NP : 1));  // one arrival per warp
+        }
+        *bad = 0;
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kTcCols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    // Bounded wait; false once this or another role has given up.
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        set_error(p.err, ERR_TIMEOUT);
+    };
+    auto wait = [&](int i, uint32_t parity) -> bool {
+        const uint32_t b = bar(i);
+        if (mbar_try_wait(b, parity)) return true;
+        if (*abort_flag) return false;
+        const uint64_t start = global_timer_ns();
+        for (uint32_t it = 1;; ++it) {
+            if (mbar_try_wait(b, parity)) return true;
+            if ((it & 63u) == 0u) {
+                if (*abort_flag) return false;
+                if (global_timer_ns() - start > p.wait_limit_ns) {
+                    give_up();
+                    return false;
+                }
+            }
+        }
+    };
+
+    float oacc[32];                                    // math threads: 32 dimensions of one query row
+    const int q4 = warp & 3, ml = q4 * 32 + lane;      // TMEM lane quarter and lane of this thread
+    const int hf = (warp - MMAW - 1) >> 2;             // math warps: tokens [32 hf, 32 hf + 32) of a tile
+    const int sub = lane >> 4;                         // math threads: which 16 of them / of the dimensions
+    const int row = 4 * (lane & 15) + q4;              // math threads: the query row of lane ml
+
+    if (warp < NP) {
+        // ---- producer warp u: lane 0 copies box u of tile j into stage j % ST once the MMAs of
+        // tile j - ST are done.  The warp loads the table entries of 32 boxes (8 tiles) a batch
+        // ahead: lane l holds box 32 b + l.
+        const int u = warp;
+        const int32_t* trow = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
+        const int bs = p.block_size, bshift = p.block_shift;
+        auto block_index = [&](int tok) { return bshift >= 0 ? (tok >> bshift) : (tok / bs); };
+        auto block_offset = [&](int tok) { return bshift >= 0 ? (tok & (bs - 1)) : (tok % bs); };
+        auto batch = [&](int b) {  // entry of box 32 b + lane (0 past the sequence)
+            const int tok = (32 * b + lane) * kTileTokens;
+            return tok < L ? __ldg(trow + block_index(tok)) : 0;
+        };
+        constexpr int TPB = 32 / SUB;  // tiles per batch
+        const uint64_t policy = l2_policy_evict_first();
+        int ent_cur = batch(0), ent_nxt = batch(1);
+        int issued = 0;
+        for (int j = 0; j < nt; ++j) {
+            if (j > 0 && j % TPB == 0) {
+                ent_cur = ent_nxt;
+                ent_nxt = batch(j / TPB + 1);
+            }
+            const int e = __shfl_sync(FULL_MASK, ent_cur, (j % TPB) * SUB + u);
+            const int s = j % ST;
+            bool ok = true;
+            if (lane == 0 && j >= ST) ok = wait(EMPTY + s, ((j / ST) - 1) & 1);
+            if (!__shfl_sync(FULL_MASK, ok ? 1 : 0, 0)) break;
+            if (lane == 0) {
+                const int tok = j * TOK + u * kTileTokens;
+                const bool live = tok < L;
+                const bool good = live && e >= 0 && (long long)e < p.num_blocks;
+                if (live && !good) {
+                    *bad = 1;
+                    set_error(p.err, ERR_BOUNDS);
+                }
+                const uint32_t full = bar(FULL + s);
+                mbar_arrive_expect_tx(full, good ? 4 * kTileTokens * 128 : 0);
+                if (good) {
+                    const int y = (e * Hkv + kvh) * bs + block_offset(tok);
+                    const uint32_t at = sbase + uint32_t(Lay::STAGES + s * Lay::STAGE + u * kTileTokens * 128);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        tma_load_2d(at + hh * Lay::KVHALF, &tmap_k, hh * 64, y, full, policy);
+                        tma_load_2d(at + (2 + hh) * Lay::KVHALF, &tmap_v, hh * 64, y, full, policy);
+                    }
+                }
+            }
+            ++issued;
+        }
+        // the CTA may not end with copies in flight: wait for the last one of each stage
+        if (lane == 0)
+            for (int s = 0; s < ST && s < issued; ++s) {
+                const int jl = s + ST * ((issued - 1 - s) / ST);
+                mbar_wait_bounded(bar(FULL + s), (jl / ST) & 1, p.wait_limit_ns);
+            }
+        __syncwarp();
+    } else if (warp == MMAW) {
+        // ---- MMA issuer: whichever of O(jp) and S(js) is ready, O first (it frees a stage)
+        constexpr uint32_t IDESC_S = umma_idesc_bf16(128, TOK, 0, 0);
+        constexpr uint32_t IDESC_O = umma_idesc_bf16(128, D, 0, 1);
+        __syncwarp();
+        const bool qok = __all_sync(FULL_MASK, wait(QREADY, 0));
+        (void)qok;
+        tc_fence_after_sync();
+        int js = 0, jp = 0;
+        uint64_t idle_since = 0;
+        bool idle = false;
+        while (jp < nt) {
+            int act = 0;  // 1: O(jp), 2: S(js), -1: give up
+            if (lane == 0) {
+                // O(jp): its probabilities are written, and the math warps have read O(jp - 2)
+                if (jp < js && mbar_test_wait(bar(PFULL + (jp & 1)), (jp >> 1) & 1) &&
+                    (jp < 2 || mbar_test_wait(bar(OFREE + (jp & 1)), ((jp >> 1) - 1) & 1)))
+                    act = 1;
+                // S(js): its tile has landed, and O(js - 2) -- the last reader of the buffer -- is complete
+                else if (js < nt && mbar_test_wait(bar(FULL + js % ST), (js / ST) & 1) &&
+                         (js < 2 || (jp >= js - 1 && mbar_test_wait(bar(OFULL + (js & 1)), ((js >> 1) - 1) & 1))))
+                    act = 2;
+                else if (*abort_flag) act = -1;
+                else if (!idle) {
+                    idle = true;
+                    idle_since = global_timer_ns();
+                } else if (global_timer_ns() - idle_since > p.wait_limit_ns) {
+                    give_up();
+                    act = -1;
+                }
+                if (act != 0) idle = false;
+            }
+            act = __shfl_sync(FULL_MASK, act, 0);
+            if (act < 0) break;
+            if (act == 0) continue;
+            if (act == 2) {
+                const int s = js % ST;
+                const int nvalid = min(TOK, L - js * TOK);
+                if (nvalid < TOK) {
+                    // rows past the sequence hold other data (or poison): zero V there so 0 * V stays 0
+                    unsigned char* v = smem + Lay::STAGES + s * Lay::STAGE + 2 * Lay::KVHALF;
+                    for (int e = lane; e < (TOK - nvalid) * 16; e += 32) {
+                        const int r = nvalid + (e >> 4), c = e & 15;
+                        *reinterpret_cast<uint4*>(v + (c >> 3) * Lay::KVHALF + r * 128 + (c & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                tc_fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t ka = sbase + uint32_t(Lay::STAGES + s * Lay::STAGE);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)  // 16 dims: 8 TMEM columns of Q, 32 bytes into the swizzled row
+                        umma_bf16_tmem_a(tmem + TS(js & 1), tmem + TQ + uint32_t(kk * 8),
+                                         umma_desc_sw128(ka + (kk >> 2) * Lay::KVHALF + (kk & 3) * 32, 16, 1024),
+                                         IDESC_S, kk > 0);
+                    umma_commit(bar(SFULL + (js & 1)));
+                }
+                ++js;
+            } else {
+                tc_fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t va = sbase + uint32_t(Lay::STAGES + (jp % ST) * Lay::STAGE + 2 * Lay::KVHALF);
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int kk = 0; kk < TOK / 16; ++kk)  // 16 tokens: 8 TMEM columns of P, 2 KiB of V
+                            umma_bf16_tmem_a(tmem + TO(jp & 1), tmem + TS(jp & 1) + uint32_t(32 * part + 8 * kk),
+                                             umma_desc_sw128(va + kk * 16 * 128, Lay::KVHALF, 1024), IDESC_O,
+                                             (part | kk) != 0);
+                    umma_commit(bar(OFULL + (jp & 1)));
+                    umma_commit(bar(EMPTY + jp % ST));
+                }
+                ++jp;
+            }
+            __syncwarp();
+        }
+        // tensor memory is released only after every MMA of this CTA is complete
+        if (lane == 0) {
+            umma_commit(bar(DONE));
+            mbar_wait_bounded(bar(DONE), 0, p.wait_limit_ns);
+        }
+        __syncwarp();
+    } else {
+        // ---- math warps
+        const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16);  // this warp's TMEM lane quarter
+        const bool rows_here = q4 < RR;                        // warp-uniform: the quarter holds a row
+        const bool is_row = row < RR;
+        // query row of this lane into TMEM: this warp's 64 dimensions, two bf16 per column
+        {
+            uint32_t w[32];
+            if (is_row) {
+                const int j = row / G, h = row - (row / G) * G;
+                const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D + 64 * hf);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = __ldg(src + c);
+                    w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) w[c] = 0u;
+            }
+            uint32_t w0[16], w1[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) { w0[c] = w[c]; w1[c] = w[16 + c]; }
+            tmem_st_x16(tl + TQ + uint32_t(32 * hf), w0);
+            tmem_st_x16(tl + TQ + uint32_t(32 * hf + 16), w1);
+            tmem_st_wait();
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(QREADY));
+
+        const int lim = is_row ? L - Q + row / G + 1 : 0;  // tokens t < lim are visible to the row
+        float m_run = -INFINITY, l_part = 0.f, al_prev = 0.f;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) oacc[c] = 0.f;
+
+        // O(i): add this thread's 32 dimensions, the running sums rescaled by the row's factor al
+        auto accumulate = [&](int i, float al) {
+            wait(OFULL + (i & 1), (i >> 1) & 1);
+            __syncwarp();
+            tc_fence_after_sync();
+            if (rows_here) {
+#pragma unroll
+                for (int s2 = 0; s2 < 2; ++s2) {
+                    uint32_t v[32];
+                    tmem_ld_x32(tl + TO(i & 1) + uint32_t(64 * hf + 32 * s2), v);
+                    if (sub == s2) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) oacc[c] = fmaf(oacc[c], al, __uint_as_float(v[c]));
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(OFREE + (i & 1)));
+        };
+
+        for (int j = 0; j < nt; ++j) {
+            wait(SFULL + (j & 1), (j >> 1) & 1);
+            __syncwarp();
+            tc_fence_after_sync();
+            float al = 0.f;
+            if (rows_here) {
+                uint32_t v[32];
+                tmem_ld_x32(tl + TS(j & 1) + uint32_t(32 * hf), v);  // scores of tokens [32 hf, 32 hf + 32)
+                const int t0 = j * TOK + 32 * hf + 16 * sub;       // this thread's 16 tokens: t0 .. t0 + 15
+                float y[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) y[c] = __uint_as_float(sub ? v[16 + c] : v[c]) * p.scale_log2;
+                if (t0 + 16 > lim) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        if (t0 + c >= lim) y[c] = -INFINITY;
+                }
+                float mx4[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mx4[c] = fmaxf(fmaxf(y[c], y[c + 4]), fmaxf(y[c + 8], y[c + 12]));
+                float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));  // the lane with the other 16 tokens
+                pmax[hf * 128 + ml] = mx;
+                // both warps of the quarter have read their scores before either writes P over them
+                tc_fence_before_sync();
+                asm volatile("bar.sync %0, 64;" ::"r"(2 + q4) : "memory");
+                tc_fence_after_sync();
+                const float mo = pmax[(hf ^ 1) * 128 + ml];
+                const float mn = fmaxf(m_run, fmaxf(mx, mo));
+                const float ref = mn == -INFINITY ? 0.f : mn;
+                al = exp2_approx(m_run - ref);
+                m_run = mn;
+                uint32_t ph[8], pl[8];
+                float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float a = exp2_approx(y[2 * e] - ref), b = exp2_approx(y[2 * e + 1] - ref);
+                    ps0 += a;
+                    ps1 += b;
+                    ph[e] = pack_bf16x2(a, b);
+                    pl[e] = pack_bf16x2(a - __uint_as_float(ph[e] << 16), b - __uint_as_float(ph[e] & 0xffff0000u));
+                }
+                l_part = l_part * al + (ps0 + ps1);
+                // both lanes of the pair write the pair's 32 tokens: [lane 0-15 part, lane 16-31 part]
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t o = __shfl_xor_sync(FULL_MASK, ph[e], 16);
+                    w[e] = sub ? o : ph[e];
+                    w[8 + e] = sub ? ph[e] : o;
+                }
+                tmem_st_x16(tl + TS(j & 1) + uint32_t(16 * hf), w);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t o = __shfl_xor_sync(FULL_MASK, pl[e], 16);
+                    w[e] = sub ? o : pl[e];
+                    w[8 + e] = sub ? pl[e] : o;
+                }
+                tmem_st_x16(tl + TS(j & 1) + uint32_t(32 + 16 * hf), w);
+                tmem_st_wait();
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(PFULL + (j & 1)));
+            if (j >= 1) accumulate(j - 1, al_prev);
+            al_prev = al;
+        }
+        if (nt >= 1) accumulate(nt - 1, al_prev);
+        l_part += __shfl_xor_sync(FULL_MASK, l_part, 16);
+        if (is_row && sub == 0) lsum[hf * NR + row] = l_part;
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 0) tmem_dealloc(tmem, kTcCols);
+    if (warp > MMAW && row < RR) {
+        const bool failed = *bad != 0 || *abort_flag != 0;
+        const float l = lsum[row] + lsum[NR + row];
+        const float inv = l == 0.f ? 0.f : 1.f / l;  // no token: 0; a NaN input stays NaN
+        float4* dst = reinterpret_cast<float4*>(out_row(row) + 64 * hf + 32 * sub);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            dst[c] = failed ? make_float4(NAN, NAN, NAN, NAN)
+                            : make_float4(oacc[4 * c] * inv, oacc[4 * c + 1] * inv, oacc[4 * c + 2] * inv,
+                                          oacc[4 * c + 3] * inv);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -848,11 +1353,11 @@ static cudaError_t launch_multi(const CUtensorMap& mk, const CUtensorMap& mv, co
     return cudaGetLastError();
 }
 
-template <int D, int MT, int NG, int NST, int OPT>
+template <int D, int MT, int NG, int NST, int OPT, int NPW>
 static cudaError_t launch_multi_wide(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p,
                                      cudaStream_t stream) {
     using Lay = WideLayout<D, NST, (OPT & kWideQs) ? MT * NG : 0>;
-    auto kern = paged_multi_query_wide_kernel<D, MT, NG, NST, OPT>;
+    auto kern = paged_multi_query_wide_kernel<D, MT, NG, NST, OPT, NPW>;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -864,7 +1369,25 @@ static cudaError_t launch_multi_wide(const CUtensorMap& mk, const CUtensorMap& m
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     const long long grid = (long long)p.num_seqs * p.num_kv_heads;
-    kern<<<unsigned(grid), (MT * NG + 1) * 32, Lay::ALLOC, stream>>>(mk, mv, p);
+    kern<<<unsigned(grid), (MT * NG + NPW) * 32, Lay::ALLOC, stream>>>(mk, mv, p);
+    return cudaGetLastError();
+}
+
+static cudaError_t launch_multi_tc(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p,
+                                   cudaStream_t stream) {
+    auto kern = paged_multi_query_tc_kernel;
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit == 0 || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcLayout::ALLOC);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const long long grid = (long long)p.num_seqs * p.num_kv_heads;
+    kern<<<unsigned(grid), kTcThreads, TcLayout::ALLOC, stream>>>(mk, mv, p);
     return cudaGetLastError();
 }
 
@@ -873,9 +1396,10 @@ static cudaError_t launch_multi_any(const CUtensorMap& mk, const CUtensorMap& mv
                                     cudaStream_t stream) {
     if (p.rows <= kMultiMaxRows) return launch_multi<D>(mk, mv, p, stream);
     switch ((p.rows + 15) / 16) {
-        case 2: return launch_multi_wide<D, 2, 2, PF_WIDE_NST_2, PF_WIDE_OPT_2>(mk, mv, p, stream);  // two groups
-        case 3: return launch_multi_wide<D, 3, 1, PF_WIDE_NST_3, PF_WIDE_OPT_3>(mk, mv, p, stream);
-        default: return launch_multi_wide<D, 4, 1, PF_WIDE_NST_4, PF_WIDE_OPT_4>(mk, mv, p, stream);
+        // producer warps: two where the consumers' registers allow (the 32-row variant), else one
+        case 2: return launch_multi_wide<D, 2, 2, PF_WIDE_NST_2, PF_WIDE_OPT_2, 2>(mk, mv, p, stream);  // two groups
+        case 3: return launch_multi_wide<D, 3, 1, PF_WIDE_NST_3, PF_WIDE_OPT_3, 1>(mk, mv, p, stream);
+        default: return launch_multi_wide<D, 4, 1, PF_WIDE_NST_4, PF_WIDE_OPT_4, 1>(mk, mv, p, stream);
     }
 }
 
@@ -883,12 +1407,13 @@ static cudaError_t launch_multi_any(const CUtensorMap& mk, const CUtensorMap& mv
 
 using namespace pf;
 
-extern "C" pf_status pf_paged_attention_multi_query(const void* q, const void* k_cache, const void* v_cache,
-                                                    const int32_t* block_tables, const int32_t* context_lens,
-                                                    int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
-                                                    int head_dim, int block_size, int max_blocks_per_seq,
-                                                    int64_t num_blocks, float scale, float* out,
-                                                    pf_stream_t stream) {
+// Host checks and parameters shared by both multi-query entry points; on success the two
+// tensor maps and the parameter block are ready to launch.
+static pf_status multi_query_setup(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int q_len,
+                                   int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                   int max_blocks_per_seq, int64_t num_blocks, float scale, float* out,
+                                   CUtensorMap* mk, CUtensorMap* mv, MultiParams* pp) {
     if (num_seqs < 0 || q_len <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         max_blocks_per_seq <= 0 || num_blocks <= 0 || !std::isfinite(scale) || num_q_heads % num_kv_heads != 0 ||
         num_blocks > INT32_MAX)
@@ -899,17 +1424,17 @@ extern "C" pf_status pf_paged_attention_multi_query(const void* q, const void* k
     if ((long long)group * q_len > kWideMaxRows) return PF_ERR_UNSUPPORTED;
     const long long rows = num_blocks * num_kv_heads * (long long)block_size;
     if (rows > INT32_MAX || (long long)num_seqs * num_kv_heads > INT32_MAX) return PF_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return PF_OK;
     auto al = [](const void* ptr, size_t a) { return ptr != nullptr && reinterpret_cast<uintptr_t>(ptr) % a == 0; };
-    if (!al(q, 16) || !al(k_cache, 16) || !al(v_cache, 16) || !al(block_tables, 4) || !al(context_lens, 4) ||
-        !al(out, 16))
+    if (num_seqs > 0 && (!al(q, 16) || !al(k_cache, 16) || !al(v_cache, 16) || !al(block_tables, 4) ||
+                         !al(context_lens, 4) || !al(out, 16)))
         return PF_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PF_OK;
     unsigned* err = nullptr;
     if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
-    CUtensorMap mk, mv;
-    if (!encode_cache_map(&mk, k_cache, rows, head_dim) || !encode_cache_map(&mv, v_cache, rows, head_dim))
+    if (!encode_cache_map(mk, k_cache, rows, head_dim) || !encode_cache_map(mv, v_cache, rows, head_dim))
         return PF_ERR_CUDA;
-    MultiParams p{};
+    MultiParams& p = *pp;
+    p = MultiParams{};
     p.q = static_cast<const uint16_t*>(q);
     p.block_tables = block_tables;
     p.context_lens = context_lens;
@@ -928,7 +1453,40 @@ extern "C" pf_status pf_paged_attention_multi_query(const void* q, const void* k
     p.block_shift = (block_size & (block_size - 1)) == 0 ? __builtin_ctz(unsigned(block_size)) : -1;
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.sorted = num_seqs > 1 && num_seqs <= kMultiSortMax;
+    return PF_OK;
+}
+
+extern "C" pf_status pf_paged_attention_multi_query(const void* q, const void* k_cache, const void* v_cache,
+                                                    const int32_t* block_tables, const int32_t* context_lens,
+                                                    int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                                    int head_dim, int block_size, int max_blocks_per_seq,
+                                                    int64_t num_blocks, float scale, float* out,
+                                                    pf_stream_t stream) {
+    CUtensorMap mk, mv;
+    MultiParams p;
+    const pf_status st = multi_query_setup(q, k_cache, v_cache, block_tables, context_lens, num_seqs, q_len,
+                                           num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                           num_blocks, scale, out, &mk, &mv, &p);
+    if (st != PF_OK || num_seqs == 0) return st;
     const cudaError_t e = head_dim == 64 ? launch_multi_any<64>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream))
                                          : launch_multi_any<128>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
+}
+
+extern "C" pf_status pf_paged_attention_multi_query_tcgen05(const void* q, const void* k_cache, const void* v_cache,
+                                                            const int32_t* block_tables, const int32_t* context_lens,
+                                                            int num_seqs, int q_len, int num_q_heads,
+                                                            int num_kv_heads, int head_dim, int block_size,
+                                                            int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                                            float* out, pf_stream_t stream) {
+    CUtensorMap mk, mv;
+    MultiParams p;
+    const pf_status st = multi_query_setup(q, k_cache, v_cache, block_tables, context_lens, num_seqs, q_len,
+                                           num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                           num_blocks, scale, out, &mk, &mv, &p);
+    if (st != PF_OK) return st;
+    if (head_dim != 128) return PF_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PF_OK;
+    const cudaError_t e = launch_multi_tc(mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }

@@ -54,24 +54,25 @@ def test_decode_step_in_a_graph(pf):
 def test_multi_query_in_a_graph(pf):
     wl = make_workload("graphmq", 4, 32, 8, 128, 16, [40, 100, 260, 33], seed=92, pool_scale=2)
     d = to_device(wl)
-    for q_len in (4, 8):   # the 16-row kernel and the wide one
+    # the 16-row kernel, the wide one and the tcgen05 form
+    for q_len, kernel in ((4, "mma"), (8, "mma"), (8, "tcgen05")):
         qt = torch.from_numpy(np.ascontiguousarray(multi_query(wl, q_len)).view(np.int16)).view(
             torch.bfloat16).cuda()
         out = torch.empty((wl.num_seqs, q_len, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device="cuda")
         args = (qt, d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"])
-        pf.paged_attention_multi_query(*args, out=out)
+        pf.paged_attention_multi_query(*args, out=out, kernel=kernel)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
             with torch.cuda.graph(g, stream=s):
-                pf.paged_attention_multi_query(*args, out=out)
+                pf.paged_attention_multi_query(*args, out=out, kernel=kernel)
         torch.cuda.current_stream().wait_stream(s)
         qt.copy_(torch.randn(tuple(qt.shape), device="cuda").to(torch.bfloat16))
         g.replay()
         torch.cuda.synchronize()
         assert pf.get_device_error() == pf.PF_OK
         got = out.clone()
-        ref = pf.paged_attention_multi_query(*args)
+        ref = pf.paged_attention_multi_query(*args, kernel=kernel)
         assert torch.equal(got, ref)
