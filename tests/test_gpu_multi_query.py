@@ -28,6 +28,7 @@ CASES = [
     (32, 8, 128, 16, 8), (32, 8, 128, 16, 16), (16, 8, 128, 32, 12),   # 32, 64 and 24 rows per kv head
     (32, 4, 64, 16, 6), (8, 8, 128, 16, 40), (4, 4, 64, 32, 64),       # 48 rows at D=64; MHA chunks of 40, 64
     (32, 8, 128, 16, 5), (16, 16, 128, 16, 3), (32, 8, 128, 48, 13),   # 20, 3 and 52 rows; a 48-token block
+    (16, 4, 64, 16, 6), (8, 8, 64, 32, 20),                            # 24 and 20 rows at D=64 (two groups)
 ]
 # the tcgen05 form is D = 128 only
 KERNEL_CASES = [c + ("mma",) for c in CASES] + [c + ("tcgen05",) for c in CASES if c[2] == 128]
