@@ -34,6 +34,7 @@
 
 #include "pf.h"
 #include "pf_device.cuh"
+#include "pf_tcgen05.cuh"
 #include "pf_internal.h"
 
 namespace pf {
@@ -872,69 +873,72 @@ __global__ void __launch_bounds__((MT * NG + NPW) * 32, 2) paged_multi_query_wid
 // 17 to 64 query rows per kv head at D = 128, with the scores and the P.V product
 // both on the fifth-generation tensor cores (single-CTA tcgen05.mma, fp32
 // accumulators in tensor memory).  One CTA per (sequence, kv head), thirteen warps,
-// one CTA per SM (by its shared memory), all 512 TMEM columns: the query rows (64
-// columns, bf16 pairs), two score buffers of 64 columns that the probabilities P
-// overwrite in place, and two 128-column buffers for one tile's P.V.
-//  * warps 0-3 stream the sequence in tiles of 64 tokens through a 6-deep ring: warp u
-//    copies the tile's u-th 16-token box of K and of V (TMA tensor copies with the
-//    128-byte swizzle, issued by lane 0) and fetches the block-table entries 32 boxes at
-//    a time, a batch ahead.  The blocks of a sequence lie anywhere in the pool, and one
-//    thread's copies to scattered pages are served one after another, so four issuing
-//    warps are what keeps enough bytes in flight;
+// one CTA per SM (by its shared memory), all 512 TMEM columns.  The tiles of 64 tokens
+// alternate between two chains, so that one chain's softmax runs while the tensor core
+// works for the other: tile j belongs to chain c = j % 2, which has a 64-column score
+// buffer that its probabilities P overwrite in place and a 128-column O accumulator.
+//  * warps 0-3 stream the sequence through a 6-deep ring: warp u copies the tile's u-th
+//    16-token box of K and of V (TMA tensor copies with the 128-byte swizzle, issued by
+//    lane 0) and fetches the block-table entries 32 boxes at a time, a batch ahead.  The
+//    blocks of a sequence lie anywhere in the pool, and one thread's copies to scattered
+//    pages are served one after another, so four issuing warps keep enough bytes in flight;
 //  * warp 4, lane 0 issues, as soon as each is ready, S(j) = Q K(j)^T -- M = 128 TMEM
-//    lanes (the query rows, each twice), N = 64 tokens, K = D; Q from tensor memory, K
-//    K-major straight from the swizzled stage -- and O(j) = P(j) V(j) -- M = 128, N = D,
-//    K = 64 tokens; P from tensor memory, V MN-major from the stage -- twice, for P's
-//    bf16 hi and lo parts;
-//  * warps 5-12, two per TMEM lane quarter (a warp may only read its quarter).  Query
-//    row r sits in lanes 32 (r % 4) + r / 4 and 16 above it, so every quarter holds 16
-//    rows twice and the work is spread over the four SM sub-partitions.  For a tile, the
-//    four threads that see row r (a lane pair in each of the quarter's two warps) each
-//    take 16 of the 64 scores, combine their maxima, run the fp32 online softmax and
-//    write the pair's 32 probabilities, as bf16 hi and lo parts, over the scores they
-//    read.  For the tile's O they each add 32 of the row's 128 dimensions into registers,
-//    rescaled by the row's factor, which every one of them holds, and write those
-//    outputs at the end.
-// The scores of one tile and the P.V product of the previous one run on the tensor
-// cores while the softmax runs on the CUDA cores.  Every wait is bounded; one that
-// gives up raises an abort flag that ends the others at once, and every role still
-// runs all its iterations, so the CTA stays in step and releases its tensor memory.
+//    lanes (the query rows, each twice), N = 64 tokens, K = D; Q from tensor memory (64
+//    columns of bf16 pairs), K K-major straight from the swizzled stage; once the chain's
+//    previous P.V is complete -- and O_c += P(j) V(j) -- M = 128, N = D, K = 64 tokens; P
+//    from tensor memory, V MN-major from the stage -- twice, for P's bf16 hi and lo parts;
+//  * warps 5-12: the four warps of chain c (one per TMEM lane quarter; a warp may only
+//    read its quarter) run its softmax.  Query row r sits in lanes 32 (r % 4) + r / 4 and 16
+//    above it, so every quarter holds 16 rows twice and the work is spread over the four
+//    SM sub-partitions; each of a row's two lanes takes 32 of the tile's tokens, they share
+//    the tile maximum through a shuffle, and each writes P for its own tokens (zeros for the
+//    other's) into its own lane: the row's two lanes of O then hold partial sums.  A row's
+//    reference maximum moves only when a score exceeds it by more than 2^8 (the
+//    probabilities stay <= 256), and then the warp rescales its O rows in place, which is
+//    safe because the chain's previous P.V is complete by then.  At the end the four
+//    partial rows of each query row (two lanes, two chains) are weighted by their chain's
+//    maximum, summed through shared memory and normalised.
+// Every wait is bounded; one that gives up raises an abort flag that ends the others at
+// once, and every role still runs all its iterations, so the CTA stays in step and
+// releases its tensor memory.
 constexpr int kTcTok = 64;        // tokens per tile
 constexpr int kTcStages = 6;      // K/V ring depth
 constexpr int kTcRows = 64;       // query rows per kv head
 constexpr int kTcCols = 512;      // TMEM columns
 constexpr int kTcProducers = 4;   // issuing warps, one per 16-token box of a tile
 constexpr int kTcThreads = 32 * (kTcProducers + 1 + 8);
+constexpr float kTcRescale = 8.f; // a reference maximum moves when a score exceeds it by more (log2 units)
 
 struct TcLayout {
     static constexpr int KVHALF = kTcTok * 128;       // 64 tokens x 64 dims of bf16
     static constexpr int STAGE = 4 * KVHALF;          // K dims [0,64), [64,128); V the same
     static constexpr int STAGES = 0;
-    static constexpr int NBARS = 2 * kTcStages + 10;
+    static constexpr int OPART = STAGES;              // after the last MMA: [2 chains][128 lanes][128] fp32 partial rows
+    static constexpr int NBARS = 2 * kTcStages + 8;
     static constexpr int BARS = STAGES + kTcStages * STAGE;
-    static constexpr int PMAX = BARS + ((NBARS * 8 + 15) / 16) * 16;  // [2 halves][128 lanes] partial maxima
-    static constexpr int LSUM = PMAX + 2 * 128 * 4;                   // [2 halves][64] partial row sums
-    static constexpr int MISC = LSUM + 2 * kTcRows * 4;               // TMEM base, bad-block flag, abort flag
+    static constexpr int STATS = BARS + ((NBARS * 8 + 15) / 16) * 16;  // [2 chains][64 rows][max, sum]
+    static constexpr int MISC = STATS + 2 * kTcRows * 2 * 4;          // TMEM base, bad-block flag, abort flag
     static constexpr int BYTES = MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;                        // room to align to 1024
+    static_assert(2 * 128 * 128 * 4 <= kTcStages * STAGE, "the partial rows fit in the stage ring");
 };
 
 __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v, const MultiParams p) {
     constexpr int D = 128, NT = kTcThreads, TOK = kTcTok, ST = kTcStages, NR = kTcRows;
     constexpr int SUB = TOK / kTileTokens;  // 16-token boxes per tile
-    constexpr int NMW = 8;                  // math warps
+    constexpr int NMW = 8, WPC = 4;         // math warps, per chain
     constexpr int NP = kTcProducers, MMAW = kTcProducers;  // producer warps 0 .. NP-1, then the MMA warp
     static_assert(NP == SUB, "one producer warp per box of a tile");
-    // TMEM columns: query rows, score / probability buffer b, P.V buffer b
+    // TMEM columns: query rows, score / probability buffer of chain c, O accumulator of chain c
     constexpr uint32_t TQ = 0;
-    auto TS = [](int b) { return uint32_t(64 + 64 * b); };
-    auto TO = [](int b) { return uint32_t(256 + 128 * b); };
+    auto TS = [](int c) { return uint32_t(64 + 64 * c); };
+    auto TO = [](int c) { return uint32_t(256 + 128 * c); };
     using Lay = TcLayout;
-    // mbarriers: K/V ring full / empty, scores ready, probabilities ready, P.V ready, P.V
-    // read, query rows stored, all MMAs done
-    enum { FULL = 0, EMPTY = ST, SFULL = 2 * ST, PFULL = SFULL + 2, OFULL = PFULL + 2, OFREE = OFULL + 2,
-           QREADY = OFREE + 2, DONE = QREADY + 1 };
+    // mbarriers: K/V ring full / empty; per chain scores ready, probabilities ready, probabilities
+    // read (the chain's P.V is complete); query rows stored; all MMAs done
+    enum { FULL = 0, EMPTY = ST, SFULL = 2 * ST, PFULL = SFULL + 2, PFREE = PFULL + 2, QREADY = PFREE + 2,
+           DONE = QREADY + 1 };
     static_assert(DONE + 1 == Lay::NBARS, "barrier count");
 
     extern __shared__ unsigned char smem_raw[];
@@ -942,8 +946,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
     unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // swizzled operands need 1 KiB alignment
     const uint32_t sbase = smem_u32(smem);
     auto bar = [&](int i) { return sbase + uint32_t(Lay::BARS + 8 * i); };
-    float* pmax = reinterpret_cast<float*>(smem + Lay::PMAX);
-    float* lsum = reinterpret_cast<float*>(smem + Lay::LSUM);
+    float* stats = reinterpret_cast<float*>(smem + Lay::STATS);
+    float* opart = reinterpret_cast<float*>(smem + Lay::OPART);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
     volatile int* bad = reinterpret_cast<volatile int*>(smem + Lay::MISC + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::MISC + 8);
@@ -967,8 +971,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < Lay::NBARS; ++i) {
-            const bool by_warps = i == PFULL || i == PFULL + 1 || i == OFREE || i == OFREE + 1 || i == QREADY;
-            mbar_init(bar(i), by_warps ? NMW : (i < FULL + ST ? NP : 1));  // one arrival per warp
+            int count = 1;                                   // commits, and the all-done commit
+            if (i < FULL + ST) count = NP;                   // one arrival per producer warp
+            if (i == PFULL || i == PFULL + 1) count = WPC;   // the chain's math warps
+            if (i == QREADY) count = NMW;
+            mbar_init(bar(i), count);
         }
         *bad = 0;
         *abort_flag = 0;
@@ -1002,10 +1009,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
         }
     };
 
-    float oacc[32];                                    // math threads: 32 dimensions of one query row
     const int q4 = warp & 3, ml = q4 * 32 + lane;      // TMEM lane quarter and lane of this thread
-    const int hf = (warp - MMAW - 1) >> 2;             // math warps: tokens [32 hf, 32 hf + 32) of a tile
-    const int sub = lane >> 4;                         // math threads: which 16 of them / of the dimensions
+    const int ch = (warp - MMAW - 1) >> 2;             // math warps: the chain (and the half of Q they store)
+    const int sub = lane >> 4;                         // math threads: which 32 tokens of a tile
     const int row = 4 * (lane & 15) + q4;              // math threads: the query row of lane ml
 
     if (warp < NP) {
@@ -1065,7 +1071,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
             }
         __syncwarp();
     } else if (warp == MMAW) {
-        // ---- MMA issuer: whichever of O(jp) and S(js) is ready, O first (it frees a stage)
+        // ---- MMA issuer: whichever of O += P(jp) V(jp) and S(js) is ready, P.V first (it frees a stage)
         constexpr uint32_t IDESC_S = umma_idesc_bf16(128, TOK, 0, 0);
         constexpr uint32_t IDESC_O = umma_idesc_bf16(128, D, 0, 1);
         __syncwarp();
@@ -1076,15 +1082,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
         uint64_t idle_since = 0;
         bool idle = false;
         while (jp < nt) {
-            int act = 0;  // 1: O(jp), 2: S(js), -1: give up
+            int act = 0;  // 1: P.V(jp), 2: S(js), -1: give up
             if (lane == 0) {
-                // O(jp): its probabilities are written, and the math warps have read O(jp - 2)
-                if (jp < js && mbar_test_wait(bar(PFULL + (jp & 1)), (jp >> 1) & 1) &&
-                    (jp < 2 || mbar_test_wait(bar(OFREE + (jp & 1)), ((jp >> 1) - 1) & 1)))
+                // P.V(jp): its probabilities are written (and its chain's O rescaled)
+                if (jp < js && mbar_test_wait(bar(PFULL + (jp & 1)), (jp >> 1) & 1))
                     act = 1;
-                // S(js): its tile has landed, and O(js - 2) -- the last reader of the buffer -- is complete
+                // S(js): its tile has landed, and the chain's previous P.V -- the last reader of the
+                // buffer -- is complete
                 else if (js < nt && mbar_test_wait(bar(FULL + js % ST), (js / ST) & 1) &&
-                         (js < 2 || (jp >= js - 1 && mbar_test_wait(bar(OFULL + (js & 1)), ((js >> 1) - 1) & 1))))
+                         (js < 2 || mbar_test_wait(bar(PFREE + (js & 1)), ((js >> 1) - 1) & 1)))
                     act = 2;
                 else if (*abort_flag) act = -1;
                 else if (!idle) {
@@ -1134,31 +1140,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
                         for (int kk = 0; kk < TOK / 16; ++kk)  // 16 tokens: 8 TMEM columns of P, 2 KiB of V
                             umma_bf16_tmem_a(tmem + TO(jp & 1), tmem + TS(jp & 1) + uint32_t(32 * part + 8 * kk),
                                              umma_desc_sw128(va + kk * 16 * 128, Lay::KVHALF, 1024), IDESC_O,
-                                             (part | kk) != 0);
-                    umma_commit(bar(OFULL + (jp & 1)));
+                                             jp >= 2 || (part | kk) != 0);
                     umma_commit(bar(EMPTY + jp % ST));
+                    umma_commit(bar(PFREE + (jp & 1)));
                 }
                 ++jp;
             }
             __syncwarp();
         }
-        // tensor memory is released only after every MMA of this CTA is complete
+        // every MMA of the CTA is complete before O is read and tensor memory released
         if (lane == 0) {
             umma_commit(bar(DONE));
             mbar_wait_bounded(bar(DONE), 0, p.wait_limit_ns);
         }
         __syncwarp();
     } else {
-        // ---- math warps
+        // ---- math warps of chain ch
         const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16);  // this warp's TMEM lane quarter
         const bool rows_here = q4 < RR;                        // warp-uniform: the quarter holds a row
         const bool is_row = row < RR;
-        // query row of this lane into TMEM: this warp's 64 dimensions, two bf16 per column
+        // query row of this lane into TMEM: this warp's 64 dimensions (by ch), two bf16 per column
         {
             uint32_t w[32];
             if (is_row) {
                 const int j = row / G, h = row - (row / G) * G;
-                const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D + 64 * hf);
+                const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D + 64 * ch);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint4 v = __ldg(src + c);
@@ -1171,8 +1177,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
             uint32_t w0[16], w1[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) { w0[c] = w[c]; w1[c] = w[16 + c]; }
-            tmem_st_x16(tl + TQ + uint32_t(32 * hf), w0);
-            tmem_st_x16(tl + TQ + uint32_t(32 * hf + 16), w1);
+            tmem_st_x16(tl + TQ + uint32_t(32 * ch), w0);
+            tmem_st_x16(tl + TQ + uint32_t(32 * ch + 16), w1);
             tmem_st_wait();
         }
         tc_fence_before_sync();
@@ -1180,118 +1186,143 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
         if (lane == 0) mbar_arrive(bar(QREADY));
 
         const int lim = is_row ? L - Q + row / G + 1 : 0;  // tokens t < lim are visible to the row
-        float m_run = -INFINITY, l_part = 0.f, al_prev = 0.f;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) oacc[c] = 0.f;
+        float m_ref = -INFINITY, l_part = 0.f;             // the row's reference maximum; this lane's sum
 
-        // O(i): add this thread's 32 dimensions, the running sums rescaled by the row's factor al
-        auto accumulate = [&](int i, float al) {
-            wait(OFULL + (i & 1), (i >> 1) & 1);
+        for (int j = ch; j < nt; j += 2) {
+            wait(SFULL + ch, (j >> 1) & 1);
             __syncwarp();
             tc_fence_after_sync();
             if (rows_here) {
+                float y[32];  // this lane's 32 scores: tokens t0 .. t0 + 31
 #pragma unroll
                 for (int s2 = 0; s2 < 2; ++s2) {
                     uint32_t v[32];
-                    tmem_ld_x32(tl + TO(i & 1) + uint32_t(64 * hf + 32 * s2), v);
+                    tmem_ld_x32(tl + TS(ch) + uint32_t(32 * s2), v);
                     if (sub == s2) {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) oacc[c] = fmaf(oacc[c], al, __uint_as_float(v[c]));
+                        for (int c = 0; c < 32; ++c) y[c] = __uint_as_float(v[c]) * p.scale_log2;
                     }
                 }
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(OFREE + (i & 1)));
-        };
-
-        for (int j = 0; j < nt; ++j) {
-            wait(SFULL + (j & 1), (j >> 1) & 1);
-            __syncwarp();
-            tc_fence_after_sync();
-            float al = 0.f;
-            if (rows_here) {
-                uint32_t v[32];
-                tmem_ld_x32(tl + TS(j & 1) + uint32_t(32 * hf), v);  // scores of tokens [32 hf, 32 hf + 32)
-                const int t0 = j * TOK + 32 * hf + 16 * sub;       // this thread's 16 tokens: t0 .. t0 + 15
-                float y[16];
+                const int t0 = j * TOK + 32 * sub;
+                if (t0 + 32 > lim) {
 #pragma unroll
-                for (int c = 0; c < 16; ++c) y[c] = __uint_as_float(sub ? v[16 + c] : v[c]) * p.scale_log2;
-                if (t0 + 16 > lim) {
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
+                    for (int c = 0; c < 32; ++c)
                         if (t0 + c >= lim) y[c] = -INFINITY;
                 }
-                float mx4[4];
+                float mx8[8];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) mx4[c] = fmaxf(fmaxf(y[c], y[c + 4]), fmaxf(y[c + 8], y[c + 12]));
-                float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));  // the lane with the other 16 tokens
-                pmax[hf * 128 + ml] = mx;
-                // both warps of the quarter have read their scores before either writes P over them
-                tc_fence_before_sync();
-                asm volatile("bar.sync %0, 64;" ::"r"(2 + q4) : "memory");
-                tc_fence_after_sync();
-                const float mo = pmax[(hf ^ 1) * 128 + ml];
-                const float mn = fmaxf(m_run, fmaxf(mx, mo));
-                const float ref = mn == -INFINITY ? 0.f : mn;
-                al = exp2_approx(m_run - ref);
-                m_run = mn;
-                uint32_t ph[8], pl[8];
+                for (int c = 0; c < 8; ++c) mx8[c] = fmaxf(fmaxf(y[c], y[c + 8]), fmaxf(y[c + 16], y[c + 24]));
+                float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));  // the row's other lane
+                // move the reference only when a score exceeds it by more than kTcRescale
+                const bool move = mx > m_ref + kTcRescale;
+                const float al = move ? exp2_approx(m_ref - mx) : 1.f;  // -inf reference: 0
+                if (move) {
+                    l_part *= al;
+                    m_ref = mx;
+                }
+                if (j >= 2 && __any_sync(FULL_MASK, move && al != 1.f)) {
+                    // rescale this lane's O row in place (the chain's previous P.V is complete)
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t v[32];
+                        tmem_ld_x32(tl + TO(ch) + uint32_t(32 * cc), v);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * al);
+                        tmem_st_x32(tl + TO(ch) + uint32_t(32 * cc), v);
+                    }
+                }
+                const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+                uint32_t ph[16], pl[16];
                 float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < 16; ++e) {
                     const float a = exp2_approx(y[2 * e] - ref), b = exp2_approx(y[2 * e + 1] - ref);
                     ps0 += a;
                     ps1 += b;
                     ph[e] = pack_bf16x2(a, b);
                     pl[e] = pack_bf16x2(a - __uint_as_float(ph[e] << 16), b - __uint_as_float(ph[e] & 0xffff0000u));
                 }
-                l_part = l_part * al + (ps0 + ps1);
-                // both lanes of the pair write the pair's 32 tokens: [lane 0-15 part, lane 16-31 part]
-                uint32_t w[16];
+                l_part += ps0 + ps1;
+                // P of this lane's 32 tokens into its own lane, zeros where the other lane's tokens are
+                uint32_t w[32];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t o = __shfl_xor_sync(FULL_MASK, ph[e], 16);
-                    w[e] = sub ? o : ph[e];
-                    w[8 + e] = sub ? ph[e] : o;
-                }
-                tmem_st_x16(tl + TS(j & 1) + uint32_t(16 * hf), w);
+                for (int e = 0; e < 16; ++e) { w[e] = sub ? 0u : ph[e]; w[16 + e] = sub ? ph[e] : 0u; }
+                tmem_st_x32(tl + TS(ch), w);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t o = __shfl_xor_sync(FULL_MASK, pl[e], 16);
-                    w[e] = sub ? o : pl[e];
-                    w[8 + e] = sub ? pl[e] : o;
-                }
-                tmem_st_x16(tl + TS(j & 1) + uint32_t(32 + 16 * hf), w);
+                for (int e = 0; e < 16; ++e) { w[e] = sub ? 0u : pl[e]; w[16 + e] = sub ? pl[e] : 0u; }
+                tmem_st_x32(tl + TS(ch) + 32u, w);
                 tmem_st_wait();
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(PFULL + (j & 1)));
-            if (j >= 1) accumulate(j - 1, al_prev);
-            al_prev = al;
+            if (lane == 0) mbar_arrive(bar(PFULL + ch));
         }
-        if (nt >= 1) accumulate(nt - 1, al_prev);
-        l_part += __shfl_xor_sync(FULL_MASK, l_part, 16);
-        if (is_row && sub == 0) lsum[hf * NR + row] = l_part;
+
+        // ---- epilogue: all MMAs are done; weight the four partial rows of each query row
+        wait(DONE, 0);
+        __syncwarp();
+        tc_fence_after_sync();
+        const float l_row = l_part + __shfl_xor_sync(FULL_MASK, l_part, 16);
+        if (is_row && sub == 0) {
+            stats[(ch * NR + row) * 2] = m_ref;
+            stats[(ch * NR + row) * 2 + 1] = l_row;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(NMW * 32) : "memory");
+        float wgt = 0.f;  // this chain's weight for the row: 2^(m_c - M) / (sum over chains)
+        if (is_row) {
+            const float m0 = stats[row * 2], l0 = stats[row * 2 + 1];
+            const float m1 = stats[(NR + row) * 2], l1 = stats[(NR + row) * 2 + 1];
+            const float M = fmaxf(m0, m1);
+            const float s0 = M == -INFINITY ? 0.f : exp2_approx(m0 - M), s1 = M == -INFINITY ? 0.f : exp2_approx(m1 - M);
+            const float lsum = l0 * s0 + l1 * s1;
+            const float inv = lsum == 0.f ? 0.f : 1.f / lsum;  // no token: 0; a NaN input stays NaN
+            wgt = (ch == 0 ? s0 : s1) * inv;
+        }
+        if (rows_here) {
+            // a chain that had no tile never wrote its accumulator: it contributes zeros
+            float* dst = opart + (size_t(ch) * 128 + ml) * D;
+            const bool has = nt > ch;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld_x32(tl + TO(ch) + uint32_t(32 * cc), v);
+                if (!has) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) v[c] = 0u;
+                }
+#pragma unroll
+                for (int c = 0; c < 32; c += 4)
+                    *reinterpret_cast<float4*>(dst + 32 * cc + c) =
+                        make_float4(__uint_as_float(v[c]) * wgt, __uint_as_float(v[c + 1]) * wgt,
+                                    __uint_as_float(v[c + 2]) * wgt, __uint_as_float(v[c + 3]) * wgt);
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(NMW * 32) : "memory");
+        if (is_row) {
+            // dims [32 (2 ch + sub), + 32) of the row: the sum of its two lanes in both chains
+            const bool failed = *bad != 0 || *abort_flag != 0;
+            const int d0 = 32 * (2 * ch + sub);
+            const int la = ml & ~16, lb = ml | 16;
+            float4* o = reinterpret_cast<float4*>(out_row(row) + d0);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float4 v = *reinterpret_cast<const float4*>(opart + (size_t(k >> 1) * 128 + ((k & 1) ? lb : la)) * D + d0 + 4 * c);
+                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+                }
+                o[c] = failed ? make_float4(NAN, NAN, NAN, NAN) : acc;
+            }
+        }
     }
 
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     if (warp == 0) tmem_dealloc(tmem, kTcCols);
-    if (warp > MMAW && row < RR) {
-        const bool failed = *bad != 0 || *abort_flag != 0;
-        const float l = lsum[row] + lsum[NR + row];
-        const float inv = l == 0.f ? 0.f : 1.f / l;  // no token: 0; a NaN input stays NaN
-        float4* dst = reinterpret_cast<float4*>(out_row(row) + 64 * hf + 32 * sub);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-            dst[c] = failed ? make_float4(NAN, NAN, NAN, NAN)
-                            : make_float4(oacc[4 * c] * inv, oacc[4 * c + 1] * inv, oacc[4 * c + 2] * inv,
-                                          oacc[4 * c + 3] * inv);
-    }
 }
 
 // ------------------------------------------------------------------ host side
