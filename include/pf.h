@@ -207,11 +207,11 @@ PF_API pf_status pf_paged_attention_multi_query(const void* q, const void* k_cac
  * as bf16 high part plus remainder, from tensor memory) are single-CTA MMAs
  * whose operands the TMA copies straight from the cache blocks.  Results agree
  * with pf_paged_attention_multi_query to fp32 rounding.  On the Llama-3-8B-
- * shaped batch it is slower than that kernel at every row count (its K/V
- * stages are held through the whole score, softmax and P.V chain, and four
- * copy-issuing warps keep fewer bytes in flight than the mma.sync kernel's two
- * CTAs per SM); it is the tensor-memory formulation of the step, kept as an
- * alternative.
+ * shaped batch it is slower than that kernel at every row count (about 1.3 ms
+ * against 0.83-1.21 ms at 32-64 rows): per 64-token tile a CTA runs a chain of
+ * ~16 MMAs from one issuing thread and a softmax, two such chains interleaved,
+ * and a lone CTA is no faster than one in a full GPU.  It is the tensor-memory
+ * formulation of the step, kept as an alternative.
  *
  * Supported: head_dim == 128 (else PF_ERR_UNSUPPORTED); the other shapes,
  * arguments and errors as pf_paged_attention_multi_query.
