@@ -43,6 +43,8 @@ constexpr int kMultiMaxRows = 16;  // g * q_len: one m16 tile of query rows
 
 struct MultiParams {
     const uint16_t* q;          // [S, q_len, Hq, D]
+    const uint16_t* k_cache;    // [NB, Hkv, bs, D] (L2 prefetches; the copies go through the tensor maps)
+    const uint16_t* v_cache;
     const int32_t* block_tables;
     const int32_t* context_lens;
     float* out;                 // [S, q_len, Hq, D]
@@ -870,75 +872,103 @@ __global__ void __launch_bounds__((MT * NG + NPW) * 32, 2) paged_multi_query_wid
 
 // ---------------------------------------------------------------- tcgen05 variant
 //
-// 17 to 64 query rows per kv head at D = 128, with the scores and the P.V product
-// both on the fifth-generation tensor cores (single-CTA tcgen05.mma, fp32
-// accumulators in tensor memory).  One CTA per (sequence, kv head), thirteen warps,
-// one CTA per SM (by its shared memory), all 512 TMEM columns.  The tiles of 64 tokens
-// alternate between two chains, so that one chain's softmax runs while the tensor core
-// works for the other: tile j belongs to chain c = j % 2, which has a 64-column score
-// buffer that its probabilities P overwrite in place and a 128-column O accumulator.
-//  * warps 0-3 stream the sequence through a 6-deep ring: warp u copies the tile's u-th
-//    16-token box of K and of V (TMA tensor copies with the 128-byte swizzle, issued by
-//    lane 0) and fetches the block-table entries 32 boxes at a time, a batch ahead.  The
-//    blocks of a sequence lie anywhere in the pool, and one thread's copies to scattered
-//    pages are served one after another, so four issuing warps keep enough bytes in flight;
-//  * warp 4, lane 0 issues, as soon as each is ready, S(j) = Q K(j)^T -- M = 128 TMEM
-//    lanes (the query rows, each twice), N = 64 tokens, K = D; Q from tensor memory (64
-//    columns of bf16 pairs), K K-major straight from the swizzled stage; once the chain's
-//    previous P.V is complete -- and O_c += P(j) V(j) -- M = 128, N = D, K = 64 tokens; P
-//    from tensor memory, V MN-major from the stage -- twice, for P's bf16 hi and lo parts;
-//  * warps 5-12: the four warps of chain c (one per TMEM lane quarter; a warp may only
-//    read its quarter) run its softmax.  Query row r sits in lanes 32 (r % 4) + r / 4 and 16
-//    above it, so every quarter holds 16 rows twice and the work is spread over the four
-//    SM sub-partitions; each of a row's two lanes takes 32 of the tile's tokens, they share
-//    the tile maximum through a shuffle, and each writes P for its own tokens (zeros for the
-//    other's) into its own lane: the row's two lanes of O then hold partial sums.  A row's
-//    reference maximum moves only when a score exceeds it by more than 2^8 (the
-//    probabilities stay <= 256), and then the warp rescales its O rows in place, which is
-//    safe because the chain's previous P.V is complete by then.  At the end the four
-//    partial rows of each query row (two lanes, two chains) are weighted by their chain's
-//    maximum, summed through shared memory and normalised.
+// Up to 64 query rows per kv head at D = 128, with both products on the fifth-generation
+// tensor cores (single-CTA tcgen05.mma, fp32 accumulators in tensor memory), computed
+// transposed so that the 128-lane M side of every product is filled by the tile's tokens
+// or by the head dimensions and the query rows are the N side:
+//     S^T(j) = K(j) Q^T           M = 128 tokens, N = 64 rows, K = D
+//     O^T   += V(j)^T P(j)^T      M = D = 128,    N = 64 rows x {hi, lo}, K = 128 tokens
+// K(j) is the A operand straight from its swizzled stage (K-major), V(j) the A operand
+// read MN-major from its stage, Q and P^T the B operands in shared memory.  P enters the
+// product as its bf16 hi part and the bf16 remainder (N columns 0-63 and 64-127 of O^T),
+// summed at the end.  One CTA per (sequence, kv head), thirteen warps, one CTA per SM
+// (by its shared memory), 256 TMEM columns (two 64-column score buffers, O^T).
+//  * warps 0-1 stream the sequence's K tiles through a 3-deep ring and warps 2-3 its V
+//    tiles through a 2-deep one, each warp copying half of a tile's eight 16-token boxes
+//    (TMA tensor copies with the 128-byte swizzle, issued by lane 0); the blocks of a
+//    sequence lie anywhere in the pool and one thread's copies to scattered pages are
+//    served one after another, so four warps issue.  Table entries are fetched 32 boxes
+//    at a time, a batch ahead;
+//  * warp 4, lane 0 issues S^T(j) once K(j) has landed and its score buffer (j % 2) is
+//    read, and O^T += V(j)^T P(j)^T once P(j) is written and V(j) has landed, the latter
+//    first; S^T(j + 1) thus runs while the softmax of tile j does;
+//  * warps 5-12: lane l of the warp with TMEM lane quarter u (warp % 4) holds token
+//    32 u + l of the tile, and warps 5-8 / 9-12 take query rows 0-31 / 32-63.  A row's
+//    reference maximum is shared by the whole tile (the product sums over its tokens):
+//    the four warps of a row half tell each other through shared memory whether any score
+//    exceeds its reference by more than 2^8, and only then take the tile's row maxima
+//    (a shuffle transpose and shared memory), move the references and rescale those rows
+//    of O^T in place once the previous product is complete.  Each thread writes its
+//    token's P row into P^T (swizzled, MN-major) and keeps the row sums of its tokens;
+//    at the end they are summed over the tile's lanes and O^T is read, normalised and
+//    written out row by row (a warp writes 32 consecutive dimensions).
 // Every wait is bounded; one that gives up raises an abort flag that ends the others at
 // once, and every role still runs all its iterations, so the CTA stays in step and
 // releases its tensor memory.
-constexpr int kTcTok = 64;        // tokens per tile
-constexpr int kTcStages = 6;      // K/V ring depth
-constexpr int kTcRows = 64;       // query rows per kv head
-constexpr int kTcCols = 512;      // TMEM columns
-constexpr int kTcProducers = 4;   // issuing warps, one per 16-token box of a tile
-constexpr int kTcThreads = 32 * (kTcProducers + 1 + 8);
+#ifndef PF_TC_KSTAGES
+#define PF_TC_KSTAGES 3
+#endif
+#ifndef PF_TC_VSTAGES
+#define PF_TC_VSTAGES 2
+#endif
+#ifndef PF_TC_PREFETCH
+#define PF_TC_PREFETCH 0
+#endif
+constexpr int kTcTok = 128;       // tokens per tile
+constexpr int kTcKStages = PF_TC_KSTAGES;  // K ring depth
+constexpr int kTcVStages = PF_TC_VSTAGES;  // V ring depth
+constexpr int kTcPrefetch = PF_TC_PREFETCH;  // tiles ahead of the copies whose blocks are prefetched into L2 (0: none)
+constexpr int kTcRows = 64;       // query rows per kv head (the N of the score product)
+constexpr int kTcCols = 256;      // TMEM columns: score buffers [0, 64) and [64, 128), O^T [128, 256)
+static_assert(kTcPrefetch >= 0 && kTcPrefetch <= 4, "prefetched tiles lie in the current or the next table batch");
+constexpr int kTcProducers = 4;   // issuing warps: two for K, two for V
+constexpr int kTcMath = 8;        // softmax warps
+constexpr int kTcThreads = 32 * (kTcProducers + 1 + kTcMath);
 constexpr float kTcRescale = 8.f; // a reference maximum moves when a score exceeds it by more (log2 units)
 
 struct TcLayout {
-    static constexpr int KVHALF = kTcTok * 128;       // 64 tokens x 64 dims of bf16
-    static constexpr int STAGE = 4 * KVHALF;          // K dims [0,64), [64,128); V the same
-    static constexpr int STAGES = 0;
-    static constexpr int OPART = STAGES;              // after the last MMA: [2 chains][128 lanes][128] fp32 partial rows
-    static constexpr int NBARS = 2 * kTcStages + 8;
-    static constexpr int BARS = STAGES + kTcStages * STAGE;
-    static constexpr int STATS = BARS + ((NBARS * 8 + 15) / 16) * 16;  // [2 chains][64 rows][max, sum]
-    static constexpr int MISC = STATS + 2 * kTcRows * 2 * 4;          // TMEM base, bad-block flag, abort flag
+    static constexpr int HALF = kTcTok * 128;         // 128 rows of 128 bytes (64 bf16): 16 KiB
+    static constexpr int STAGE = 2 * HALF;            // one tile of K or of V: dims [0, 64), [64, 128)
+    static constexpr int KRING = 0;
+    static constexpr int VRING = KRING + kTcKStages * STAGE;
+    static constexpr int PT = VRING + kTcVStages * STAGE;  // P^T: N blocks hi, lo of [128 tokens][64 rows]
+    static constexpr int QS = PT + 2 * HALF;                // Q: dim halves of [64 rows][64 dims]
+    static constexpr int NBARS = 2 * kTcKStages + 2 * kTcVStages + 8;
+    static constexpr int BARS = QS + 2 * kTcRows * 128;
+    static constexpr int FLAGS = BARS + ((NBARS * 8 + 15) / 16) * 16;  // [2 row halves][2 tiles][4 quarters] int
+    static constexpr int RMAX = FLAGS + 2 * 2 * 4 * 4;                 // [2 row halves][32 rows][4 quarters] float
+    static constexpr int LSUM = RMAX + 2 * 32 * 4 * 4;                 // [4 quarters][64 rows] float
+    static constexpr int MREF = LSUM + 4 * kTcRows * 4;                // [8 math warps][3][32 rows] float
+    static constexpr int MISC = MREF + kTcMath * 3 * 32 * 4;           // TMEM base, bad-block flag, abort flag
     static constexpr int BYTES = MISC + 16;
-    static constexpr int ALLOC = BYTES + 1024;                        // room to align to 1024
-    static_assert(2 * 128 * 128 * 4 <= kTcStages * STAGE, "the partial rows fit in the stage ring");
+    static constexpr int ALLOC = BYTES + 1024;                         // room to align to 1024
 };
+
+// Starts pulling `bytes` (a multiple of 16) of global memory at `src` (16-byte aligned) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// fp32 <-> int32 keys whose signed order is the order of the floats (-inf lowest), for
+// the integer warp reduction.
+__device__ __forceinline__ int float_to_ordered(float f) {
+    const int i = __float_as_int(f);
+    return i ^ ((i >> 31) & 0x7FFFFFFF);
+}
+__device__ __forceinline__ float ordered_to_float(int i) { return __int_as_float(i ^ ((i >> 31) & 0x7FFFFFFF)); }
 
 __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v, const MultiParams p) {
-    constexpr int D = 128, NT = kTcThreads, TOK = kTcTok, ST = kTcStages, NR = kTcRows;
-    constexpr int SUB = TOK / kTileTokens;  // 16-token boxes per tile
-    constexpr int NMW = 8, WPC = 4;         // math warps, per chain
-    constexpr int NP = kTcProducers, MMAW = kTcProducers;  // producer warps 0 .. NP-1, then the MMA warp
-    static_assert(NP == SUB, "one producer warp per box of a tile");
-    // TMEM columns: query rows, score / probability buffer of chain c, O accumulator of chain c
-    constexpr uint32_t TQ = 0;
-    auto TS = [](int c) { return uint32_t(64 + 64 * c); };
-    auto TO = [](int c) { return uint32_t(256 + 128 * c); };
+    constexpr int D = 128, NT = kTcThreads, TOK = kTcTok, NK = kTcKStages, NV = kTcVStages, NR = kTcRows;
+    constexpr int BOXES = TOK / kTileTokens;  // 16-token boxes per tile
+    constexpr int NMW = kTcMath, MMAW = kTcProducers;
+    constexpr uint32_t TO = 128;              // O^T columns: rows 0-63 (hi), 64-127 (lo)
+    auto TS = [](int b) { return uint32_t(64 * b); };
     using Lay = TcLayout;
-    // mbarriers: K/V ring full / empty; per chain scores ready, probabilities ready, probabilities
-    // read (the chain's P.V is complete); query rows stored; all MMAs done
-    enum { FULL = 0, EMPTY = ST, SFULL = 2 * ST, PFULL = SFULL + 2, PFREE = PFULL + 2, QREADY = PFREE + 2,
-           DONE = QREADY + 1 };
+    // mbarriers: K and V rings full / empty; per score buffer written / read; P^T written /
+    // read (its product complete); Q stored; all MMAs done
+    enum { KFULL = 0, KEMPTY = NK, VFULL = 2 * NK, VEMPTY = 2 * NK + NV, SFULL = 2 * NK + 2 * NV, SFREE = SFULL + 2,
+           PFULL = SFREE + 2, PFREE = PFULL + 1, QREADY = PFREE + 1, DONE = QREADY + 1 };
     static_assert(DONE + 1 == Lay::NBARS, "barrier count");
 
     extern __shared__ unsigned char smem_raw[];
@@ -946,8 +976,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
     unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // swizzled operands need 1 KiB alignment
     const uint32_t sbase = smem_u32(smem);
     auto bar = [&](int i) { return sbase + uint32_t(Lay::BARS + 8 * i); };
-    float* stats = reinterpret_cast<float*>(smem + Lay::STATS);
-    float* opart = reinterpret_cast<float*>(smem + Lay::OPART);
+    volatile int* flags = reinterpret_cast<volatile int*>(smem + Lay::FLAGS);
+    float* rmax = reinterpret_cast<float*>(smem + Lay::RMAX);
+    float* lsum = reinterpret_cast<float*>(smem + Lay::LSUM);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
     volatile int* bad = reinterpret_cast<volatile int*>(smem + Lay::MISC + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::MISC + 8);
@@ -971,10 +1002,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < Lay::NBARS; ++i) {
-            int count = 1;                                   // commits, and the all-done commit
-            if (i < FULL + ST) count = NP;                   // one arrival per producer warp
-            if (i == PFULL || i == PFULL + 1) count = WPC;   // the chain's math warps
-            if (i == QREADY) count = NMW;
+            int count = 1;                                                 // commits
+            if ((i >= KFULL && i < KFULL + NK) || (i >= VFULL && i < VFULL + NV)) count = 2;  // two issuing warps
+            if (i == SFREE || i == SFREE + 1 || i == PFULL || i == QREADY) count = NMW;      // the math warps
             mbar_init(bar(i), count);
         }
         *bad = 0;
@@ -1009,16 +1039,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
         }
     };
 
-    const int q4 = warp & 3, ml = q4 * 32 + lane;      // TMEM lane quarter and lane of this thread
-    const int ch = (warp - MMAW - 1) >> 2;             // math warps: the chain (and the half of Q they store)
-    const int sub = lane >> 4;                         // math threads: which 32 tokens of a tile
-    const int row = 4 * (lane & 15) + q4;              // math threads: the query row of lane ml
-
-    if (warp < NP) {
-        // ---- producer warp u: lane 0 copies box u of tile j into stage j % ST once the MMAs of
-        // tile j - ST are done.  The warp loads the table entries of 32 boxes (8 tiles) a batch
+    if (warp < kTcProducers) {
+        // ---- producer warp: warps 0-1 copy K, warps 2-3 V; warp w takes boxes w % 2, + 2, + 4,
+        // + 6 of every tile.  The warp loads the table entries of 32 boxes (4 tiles) a batch
         // ahead: lane l holds box 32 b + l.
-        const int u = warp;
+        const bool is_v = warp >= 2;
+        const int pw = warp & 1;
+        const int NS = is_v ? NV : NK;
+        const int FULLB = is_v ? VFULL : KFULL, EMPTYB = is_v ? VEMPTY : KEMPTY;
+        const uint32_t ring = sbase + uint32_t(is_v ? Lay::VRING : Lay::KRING);
+        const CUtensorMap* map = is_v ? &tmap_v : &tmap_k;
         const int32_t* trow = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
         const int bs = p.block_size, bshift = p.block_shift;
         auto block_index = [&](int tok) { return bshift >= 0 ? (tok >> bshift) : (tok / bs); };
@@ -1027,7 +1057,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
             const int tok = (32 * b + lane) * kTileTokens;
             return tok < L ? __ldg(trow + block_index(tok)) : 0;
         };
-        constexpr int TPB = 32 / SUB;  // tiles per batch
+        constexpr int TPB = 32 / BOXES;  // tiles per batch
         const uint64_t policy = l2_policy_evict_first();
         int ent_cur = batch(0), ent_nxt = batch(1);
         int issued = 0;
@@ -1036,44 +1066,64 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
                 ent_cur = ent_nxt;
                 ent_nxt = batch(j / TPB + 1);
             }
-            const int e = __shfl_sync(FULL_MASK, ent_cur, (j % TPB) * SUB + u);
-            const int s = j % ST;
+            int e[BOXES / 2];
+#pragma unroll
+            for (int i = 0; i < BOXES / 2; ++i) e[i] = __shfl_sync(FULL_MASK, ent_cur, (j % TPB) * BOXES + pw + 2 * i);
+            if (kTcPrefetch > 0 && pw == 0 && j + kTcPrefetch < nt) {
+                // lanes 0-7 of the first warp of each tensor start tile j + kTcPrefetch's boxes toward L2,
+                // so that the ring's copies find them there; its entries are in this batch or the next
+                const int jt = j + kTcPrefetch, src = (jt % TPB) * BOXES + (lane & (BOXES - 1));
+                const int ec = __shfl_sync(FULL_MASK, ent_cur, src), en = __shfl_sync(FULL_MASK, ent_nxt, src);
+                const int ef = jt / TPB == j / TPB ? ec : en;
+                const int tok = jt * TOK + (lane & (BOXES - 1)) * kTileTokens;
+                if (lane < BOXES && tok < L && ef >= 0 && (long long)ef < p.num_blocks)
+                    bulk_prefetch_l2((is_v ? p.v_cache : p.k_cache) +
+                                         ((size_t(ef) * Hkv + kvh) * bs + block_offset(tok)) * D,
+                                     kTileTokens * D * 2);
+            }
+            const int s = j % NS;
             bool ok = true;
-            if (lane == 0 && j >= ST) ok = wait(EMPTY + s, ((j / ST) - 1) & 1);
+            if (lane == 0 && j >= NS) ok = wait(EMPTYB + s, ((j / NS) - 1) & 1);
             if (!__shfl_sync(FULL_MASK, ok ? 1 : 0, 0)) break;
             if (lane == 0) {
-                const int tok = j * TOK + u * kTileTokens;
-                const bool live = tok < L;
-                const bool good = live && e >= 0 && (long long)e < p.num_blocks;
-                if (live && !good) {
-                    *bad = 1;
-                    set_error(p.err, ERR_BOUNDS);
-                }
-                const uint32_t full = bar(FULL + s);
-                mbar_arrive_expect_tx(full, good ? 4 * kTileTokens * 128 : 0);
-                if (good) {
-                    const int y = (e * Hkv + kvh) * bs + block_offset(tok);
-                    const uint32_t at = sbase + uint32_t(Lay::STAGES + s * Lay::STAGE + u * kTileTokens * 128);
+                bool good[BOXES / 2];
+                uint32_t bytes = 0;
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        tma_load_2d(at + hh * Lay::KVHALF, &tmap_k, hh * 64, y, full, policy);
-                        tma_load_2d(at + (2 + hh) * Lay::KVHALF, &tmap_v, hh * 64, y, full, policy);
+                for (int i = 0; i < BOXES / 2; ++i) {
+                    const int tok = j * TOK + (pw + 2 * i) * kTileTokens;
+                    const bool live = tok < L;
+                    good[i] = live && e[i] >= 0 && (long long)e[i] < p.num_blocks;
+                    if (live && !good[i]) {
+                        *bad = 1;
+                        set_error(p.err, ERR_BOUNDS);
                     }
+                    bytes += good[i] ? 2u * kTileTokens * 128u : 0u;
+                }
+                const uint32_t full = bar(FULLB + s);
+                mbar_arrive_expect_tx(full, bytes);
+#pragma unroll
+                for (int i = 0; i < BOXES / 2; ++i) {
+                    if (!good[i]) continue;
+                    const int b = pw + 2 * i, tok = j * TOK + b * kTileTokens;
+                    const int y = (e[i] * Hkv + kvh) * bs + block_offset(tok);
+                    const uint32_t at = ring + uint32_t(s * Lay::STAGE + b * kTileTokens * 128);
+                    tma_load_2d(at, map, 0, y, full, policy);
+                    tma_load_2d(at + Lay::HALF, map, 64, y, full, policy);
                 }
             }
             ++issued;
         }
-        // the CTA may not end with copies in flight: wait for the last one of each stage
+        // the CTA may not end with copies in flight: wait for the last fill of each stage
         if (lane == 0)
-            for (int s = 0; s < ST && s < issued; ++s) {
-                const int jl = s + ST * ((issued - 1 - s) / ST);
-                mbar_wait_bounded(bar(FULL + s), (jl / ST) & 1, p.wait_limit_ns);
+            for (int s = 0; s < NS && s < issued; ++s) {
+                const int jl = s + NS * ((issued - 1 - s) / NS);
+                mbar_wait_bounded(bar(FULLB + s), (jl / NS) & 1, p.wait_limit_ns);
             }
         __syncwarp();
     } else if (warp == MMAW) {
-        // ---- MMA issuer: whichever of O += P(jp) V(jp) and S(js) is ready, P.V first (it frees a stage)
-        constexpr uint32_t IDESC_S = umma_idesc_bf16(128, TOK, 0, 0);
-        constexpr uint32_t IDESC_O = umma_idesc_bf16(128, D, 0, 1);
+        // ---- MMA issuer: whichever of O^T += V(jp)^T P(jp)^T and S^T(js) is ready, the former first
+        constexpr uint32_t IDESC_S = umma_idesc_bf16(TOK, NR, 0, 0);
+        constexpr uint32_t IDESC_O = umma_idesc_bf16(D, 2 * NR, 1, 1);
         __syncwarp();
         const bool qok = __all_sync(FULL_MASK, wait(QREADY, 0));
         (void)qok;
@@ -1084,13 +1134,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
         while (jp < nt) {
             int act = 0;  // 1: P.V(jp), 2: S(js), -1: give up
             if (lane == 0) {
-                // P.V(jp): its probabilities are written (and its chain's O rescaled)
-                if (jp < js && mbar_test_wait(bar(PFULL + (jp & 1)), (jp >> 1) & 1))
+                if (jp < js && mbar_test_wait(bar(PFULL), jp & 1) &&
+                    mbar_test_wait(bar(VFULL + jp % NV), (jp / NV) & 1))
                     act = 1;
-                // S(js): its tile has landed, and the chain's previous P.V -- the last reader of the
-                // buffer -- is complete
-                else if (js < nt && mbar_test_wait(bar(FULL + js % ST), (js / ST) & 1) &&
-                         (js < 2 || mbar_test_wait(bar(PFREE + (js & 1)), ((js >> 1) - 1) & 1)))
+                // S(js): K landed, and the softmax of tile js - 2 has read the score buffer
+                else if (js < nt && mbar_test_wait(bar(KFULL + js % NK), (js / NK) & 1) &&
+                         (js < 2 || mbar_test_wait(bar(SFREE + (js & 1)), ((js >> 1) - 1) & 1)))
                     act = 2;
                 else if (*abort_flag) act = -1;
                 else if (!idle) {
@@ -1105,216 +1154,244 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
             act = __shfl_sync(FULL_MASK, act, 0);
             if (act < 0) break;
             if (act == 0) continue;
+            tc_fence_after_sync();
             if (act == 2) {
-                const int s = js % ST;
-                const int nvalid = min(TOK, L - js * TOK);
-                if (nvalid < TOK) {
-                    // rows past the sequence hold other data (or poison): zero V there so 0 * V stays 0
-                    unsigned char* v = smem + Lay::STAGES + s * Lay::STAGE + 2 * Lay::KVHALF;
-                    for (int e = lane; e < (TOK - nvalid) * 16; e += 32) {
-                        const int r = nvalid + (e >> 4), c = e & 15;
-                        *reinterpret_cast<uint4*>(v + (c >> 3) * Lay::KVHALF + r * 128 + (c & 7) * 16) =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                }
-                __syncwarp();
-                tc_fence_after_sync();
                 if (lane == 0) {
-                    const uint32_t ka = sbase + uint32_t(Lay::STAGES + s * Lay::STAGE);
+                    const uint32_t ka = sbase + uint32_t(Lay::KRING + (js % NK) * Lay::STAGE);
+                    const uint32_t qa = sbase + uint32_t(Lay::QS);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)  // 16 dims: 8 TMEM columns of Q, 32 bytes into the swizzled row
-                        umma_bf16_tmem_a(tmem + TS(js & 1), tmem + TQ + uint32_t(kk * 8),
-                                         umma_desc_sw128(ka + (kk >> 2) * Lay::KVHALF + (kk & 3) * 32, 16, 1024),
-                                         IDESC_S, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk)  // 16 dims: 32 bytes into the swizzled rows of K and Q
+                        umma_bf16(tmem + TS(js & 1),
+                                  umma_desc_sw128(ka + (kk >> 2) * Lay::HALF + (kk & 3) * 32, 16, 1024),
+                                  umma_desc_sw128(qa + (kk >> 2) * (NR * 128) + (kk & 3) * 32, 16, 1024), IDESC_S,
+                                  kk > 0);
                     umma_commit(bar(SFULL + (js & 1)));
+                    umma_commit(bar(KEMPTY + js % NK));
                 }
                 ++js;
             } else {
-                tc_fence_after_sync();
+                const uint32_t voff = uint32_t(Lay::VRING + (jp % NV) * Lay::STAGE);
+                const int nvalid = min(TOK, L - jp * TOK);
+                if (nvalid < TOK) {
+                    // tokens past the sequence hold other data (or poison): zero V there so 0 * V stays 0
+                    for (int e = lane; e < (TOK - nvalid) * 16; e += 32) {
+                        const int r = nvalid + (e >> 4), c = e & 15;
+                        *reinterpret_cast<uint4*>(smem + voff + (c >> 3) * Lay::HALF + r * 128 + (c & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
                 if (lane == 0) {
-                    const uint32_t va = sbase + uint32_t(Lay::STAGES + (jp % ST) * Lay::STAGE + 2 * Lay::KVHALF);
+                    const uint32_t va = sbase + voff, pa = sbase + uint32_t(Lay::PT);
 #pragma unroll
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < TOK / 16; ++kk)  // 16 tokens: 8 TMEM columns of P, 2 KiB of V
-                            umma_bf16_tmem_a(tmem + TO(jp & 1), tmem + TS(jp & 1) + uint32_t(32 * part + 8 * kk),
-                                             umma_desc_sw128(va + kk * 16 * 128, Lay::KVHALF, 1024), IDESC_O,
-                                             jp >= 2 || (part | kk) != 0);
-                    umma_commit(bar(EMPTY + jp % ST));
-                    umma_commit(bar(PFREE + (jp & 1)));
+                    for (int kk = 0; kk < TOK / 16; ++kk)  // 16 tokens: 2 KiB into V and into P^T
+                        umma_bf16(tmem + TO, umma_desc_sw128(va + kk * 2048, Lay::HALF, 1024),
+                                  umma_desc_sw128(pa + kk * 2048, Lay::HALF, 1024), IDESC_O, jp > 0 || kk > 0);
+                    umma_commit(bar(VEMPTY + jp % NV));
+                    umma_commit(bar(PFREE));
                 }
                 ++jp;
             }
             __syncwarp();
         }
-        // every MMA of the CTA is complete before O is read and tensor memory released
+        // every MMA of the CTA is complete before O^T is read and tensor memory released
         if (lane == 0) {
             umma_commit(bar(DONE));
             mbar_wait_bounded(bar(DONE), 0, p.wait_limit_ns);
         }
         __syncwarp();
     } else {
-        // ---- math warps of chain ch
+        // ---- math warps
+        const int mw = warp - MMAW - 1;                        // 0 .. 7
+        const int q4 = warp & 3, hh = mw >> 2;                 // TMEM lane quarter; row half
+        const int tk = 32 * q4 + lane;                         // this thread's token of a tile, and its O^T dim
         const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16);  // this warp's TMEM lane quarter
-        const bool rows_here = q4 < RR;                        // warp-uniform: the quarter holds a row
-        const bool is_row = row < RR;
-        // query row of this lane into TMEM: this warp's 64 dimensions (by ch), two bf16 per column
-        {
-            uint32_t w[32];
-            if (is_row) {
-                const int j = row / G, h = row - (row / G) * G;
-                const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D + 64 * ch);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v = __ldg(src + c);
-                    w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 32; ++c) w[c] = 0u;
+        const int barid = 1 + hh;                              // named barrier of the row half's four warps
+
+        // Q (rows past RR zero) into its swizzled K-major tile: 1024 chunks of 16 bytes
+        for (int i = mw * 32 + lane; i < NR * 16; i += NMW * 32) {
+            const int r = i >> 4, c16 = i & 15;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < RR) {
+                const int j = r / G, h = r - (r / G) * G;
+                v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D) + c16);
             }
-            uint32_t w0[16], w1[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) { w0[c] = w[c]; w1[c] = w[16 + c]; }
-            tmem_st_x16(tl + TQ + uint32_t(32 * ch), w0);
-            tmem_st_x16(tl + TQ + uint32_t(32 * ch + 16), w1);
-            tmem_st_wait();
+            *reinterpret_cast<uint4*>(smem + Lay::QS + (c16 >> 3) * (NR * 128) + r * 128 +
+                                      (((c16 & 7) ^ (r & 7)) << 4)) = v;
         }
-        tc_fence_before_sync();
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(QREADY));
 
-        const int lim = is_row ? L - Q + row / G + 1 : 0;  // tokens t < lim are visible to the row
-        float m_ref = -INFINITY, l_part = 0.f;             // the row's reference maximum; this lane's sum
+        const int lim0 = L - Q + 1;  // row r sees the tokens t < min(L, lim0 + r / G)
+        // this warp's copy of rows 32 hh + c's reference maxima (the same in the half's four warps),
+        // and per tile the factor and the shift that moving them applies
+        float* mref = reinterpret_cast<float*>(smem + Lay::MREF) + mw * 3 * 32;
+        float* alph = mref + 32;
+        float* shft = mref + 64;
+        mref[lane] = -INFINITY;
+        __syncwarp();
+        float l_part[32];  // this token's share of the rows' sums
+#pragma unroll
+        for (int c = 0; c < 32; ++c) l_part[c] = 0.f;
+        unsigned char* prow = smem + Lay::PT + tk * 128;  // this token's 128-byte row in both N blocks of P^T
 
-        for (int j = ch; j < nt; j += 2) {
-            wait(SFULL + ch, (j >> 1) & 1);
+        for (int j = 0; j < nt; ++j) {
+            const int b = j & 1;
+            wait(SFULL + b, (j >> 1) & 1);
             __syncwarp();
             tc_fence_after_sync();
-            if (rows_here) {
-                float y[32];  // this lane's 32 scores: tokens t0 .. t0 + 31
+            float y[32];  // log2-scaled scores of rows 32 hh + c, then relative to the reference
+            {
+                uint32_t v[32];
+                tmem_ld_x32(tl + TS(b) + uint32_t(32 * hh), v);
 #pragma unroll
-                for (int s2 = 0; s2 < 2; ++s2) {
-                    uint32_t v[32];
-                    tmem_ld_x32(tl + TS(ch) + uint32_t(32 * s2), v);
-                    if (sub == s2) {
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) y[c] = __uint_as_float(v[c]) * p.scale_log2;
-                    }
-                }
-                const int t0 = j * TOK + 32 * sub;
-                if (t0 + 32 > lim) {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (t0 + c >= lim) y[c] = -INFINITY;
-                }
-                float mx8[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) mx8[c] = fmaxf(fmaxf(y[c], y[c + 8]), fmaxf(y[c + 16], y[c + 24]));
-                float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-                mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));  // the row's other lane
-                // move the reference only when a score exceeds it by more than kTcRescale
-                const bool move = mx > m_ref + kTcRescale;
-                const float al = move ? exp2_approx(m_ref - mx) : 1.f;  // -inf reference: 0
-                if (move) {
-                    l_part *= al;
-                    m_ref = mx;
-                }
-                if (j >= 2 && __any_sync(FULL_MASK, move && al != 1.f)) {
-                    // rescale this lane's O row in place (the chain's previous P.V is complete)
-#pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t v[32];
-                        tmem_ld_x32(tl + TO(ch) + uint32_t(32 * cc), v);
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * al);
-                        tmem_st_x32(tl + TO(ch) + uint32_t(32 * cc), v);
-                    }
-                }
-                const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-                uint32_t ph[16], pl[16];
-                float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float a = exp2_approx(y[2 * e] - ref), b = exp2_approx(y[2 * e + 1] - ref);
-                    ps0 += a;
-                    ps1 += b;
-                    ph[e] = pack_bf16x2(a, b);
-                    pl[e] = pack_bf16x2(a - __uint_as_float(ph[e] << 16), b - __uint_as_float(ph[e] & 0xffff0000u));
-                }
-                l_part += ps0 + ps1;
-                // P of this lane's 32 tokens into its own lane, zeros where the other lane's tokens are
-                uint32_t w[32];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) { w[e] = sub ? 0u : ph[e]; w[16 + e] = sub ? ph[e] : 0u; }
-                tmem_st_x32(tl + TS(ch), w);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) { w[e] = sub ? 0u : pl[e]; w[16 + e] = sub ? pl[e] : 0u; }
-                tmem_st_x32(tl + TS(ch) + 32u, w);
-                tmem_st_wait();
+                for (int c = 0; c < 32; ++c) y[c] = __uint_as_float(v[c]) * p.scale_log2;
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(PFULL + ch));
+            if (lane == 0) mbar_arrive(bar(SFREE + b));
+
+            const int t = j * TOK + tk;
+            if (j * TOK + TOK > lim0) {  // some row does not see some token of this tile
+                // row r sees t iff t < L and r / G >= t - lim0 + 1, i.e. r >= (t - lim0 + 1) G
+                const int rmin = t >= L ? NR : (t < lim0 ? 0 : min(NR, (t - lim0 + 1) * G));
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    if (32 * hh + c < rmin) y[c] = -INFINITY;
+            }
+            // does any score exceed its row's reference by more than the margin?  (-inf reference: any
+            // finite score); then scores relative to the reference (-inf reference: 0)
+            bool over = false;
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 m4 = *reinterpret_cast<const float4*>(mref + 4 * c4);
+                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = 4 * c4 + i;
+                    over |= y[c] > mm[i] + kTcRescale;
+                    y[c] -= mm[i] == -INFINITY ? 0.f : mm[i];
+                }
+            }
+            const bool wover = __any_sync(FULL_MASK, over);
+            if (lane == 0) flags[(hh * 2 + b) * 4 + q4] = wover ? 1 : 0;
+            asm volatile("bar.sync %0, 128;" ::"r"(barid) : "memory");
+            const bool any_over = (flags[(hh * 2 + b) * 4 + 0] | flags[(hh * 2 + b) * 4 + 1] |
+                                   flags[(hh * 2 + b) * 4 + 2] | flags[(hh * 2 + b) * 4 + 3]) != 0;
+            bool do_rescale = false;  // rows of O^T to scale by alph once the previous product is complete
+            if (any_over) {
+                // the tile's row maxima: this warp's 32 tokens by integer warp reductions (lane c: row
+                // 32 hh + c), then over the half's four warps through shared memory
+                {
+                    float mr = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int m = __reduce_max_sync(FULL_MASK, float_to_ordered(y[c]));
+                        if (lane == c) mr = ordered_to_float(m);
+                    }
+                    const float old = mref[lane];
+                    rmax[((hh * 32) + lane) * 4 + q4] = mr + (old == -INFINITY ? 0.f : old);
+                }
+                asm volatile("bar.sync %0, 128;" ::"r"(barid) : "memory");
+                {
+                    const float4 m4 = *reinterpret_cast<const float4*>(rmax + ((hh * 32) + lane) * 4);
+                    const float mx = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+                    const float old = mref[lane];
+                    const bool move = mx > old + kTcRescale;
+                    const float now = move ? mx : old;
+                    alph[lane] = move ? exp2_approx(old - mx) : 1.f;  // -inf reference: 0
+                    shft[lane] = (old == -INFINITY ? 0.f : old) - (now == -INFINITY ? 0.f : now);
+                    // the same decision in the half's four warps: their references agree
+                    do_rescale = j > 0 && __any_sync(FULL_MASK, move && old != -INFINITY);
+                    __syncwarp();
+                    mref[lane] = now;
+                    __syncwarp();
+                }
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(alph + 4 * c4);
+                    const float4 s4 = *reinterpret_cast<const float4*>(shft + 4 * c4);
+                    const float aa[4] = {a4.x, a4.y, a4.z, a4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        l_part[4 * c4 + i] *= aa[i];
+                        y[4 * c4 + i] += ss[i];
+                    }
+                }
+            }
+            // the previous product (the last reader of P^T and writer of O^T) is complete
+            if (j > 0) wait(PFREE, (j - 1) & 1);
+            // probabilities of this token for the half's 32 rows, as bf16 hi and lo parts: chunk k
+            // (rows 32 hh + 8 k ..) of each goes to 16-byte slot (4 hh + k) ^ (tk % 8) of the token's row
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t ph[4], pl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c0 = 8 * k + 2 * e;
+                    const float a = exp2_approx(y[c0]), c = exp2_approx(y[c0 + 1]);
+                    l_part[c0] += a;
+                    l_part[c0 + 1] += c;
+                    ph[e] = pack_bf16x2(a, c);
+                    pl[e] = pack_bf16x2(a - __uint_as_float(ph[e] << 16), c - __uint_as_float(ph[e] & 0xffff0000u));
+                }
+                const int slot = ((4 * hh + k) ^ (tk & 7)) << 4;
+                *reinterpret_cast<uint4*>(prow + slot) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                *reinterpret_cast<uint4*>(prow + Lay::HALF + slot) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+            }
+            if (do_rescale) {
+                __syncwarp();
+                tc_fence_after_sync();
+#pragma unroll
+                for (int part = 0; part < 4; ++part) {  // hi, lo columns of this half's rows, dim tk; 16 at a time
+                    uint32_t v[16];
+                    const uint32_t ta = tl + TO + uint32_t(64 * (part >> 1) + 32 * hh + 16 * (part & 1));
+                    tmem_ld_x16(ta, v);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alph[16 * (part & 1) + c]);
+                    tmem_st_x16(ta, v);
+                }
+                tmem_st_wait();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(PFULL));
         }
 
-        // ---- epilogue: all MMAs are done; weight the four partial rows of each query row
+        // ---- epilogue: all MMAs are done; row sums over the tile's 128 token lanes, then O^T row by row
         wait(DONE, 0);
         __syncwarp();
         tc_fence_after_sync();
-        const float l_row = l_part + __shfl_xor_sync(FULL_MASK, l_part, 16);
-        if (is_row && sub == 0) {
-            stats[(ch * NR + row) * 2] = m_ref;
-            stats[(ch * NR + row) * 2 + 1] = l_row;
-        }
-        asm volatile("bar.sync 1, %0;" ::"r"(NMW * 32) : "memory");
-        float wgt = 0.f;  // this chain's weight for the row: 2^(m_c - M) / (sum over chains)
-        if (is_row) {
-            const float m0 = stats[row * 2], l0 = stats[row * 2 + 1];
-            const float m1 = stats[(NR + row) * 2], l1 = stats[(NR + row) * 2 + 1];
-            const float M = fmaxf(m0, m1);
-            const float s0 = M == -INFINITY ? 0.f : exp2_approx(m0 - M), s1 = M == -INFINITY ? 0.f : exp2_approx(m1 - M);
-            const float lsum = l0 * s0 + l1 * s1;
-            const float inv = lsum == 0.f ? 0.f : 1.f / lsum;  // no token: 0; a NaN input stays NaN
-            wgt = (ch == 0 ? s0 : s1) * inv;
-        }
-        if (rows_here) {
-            // a chain that had no tile never wrote its accumulator: it contributes zeros
-            float* dst = opart + (size_t(ch) * 128 + ml) * D;
-            const bool has = nt > ch;
+        {
+            float l = 0.f;  // lane c: row 32 hh + c
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld_x32(tl + TO(ch) + uint32_t(32 * cc), v);
-                if (!has) {
+            for (int c = 0; c < 32; ++c) {
+                float v = l_part[c];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) v[c] = 0u;
-                }
-#pragma unroll
-                for (int c = 0; c < 32; c += 4)
-                    *reinterpret_cast<float4*>(dst + 32 * cc + c) =
-                        make_float4(__uint_as_float(v[c]) * wgt, __uint_as_float(v[c + 1]) * wgt,
-                                    __uint_as_float(v[c + 2]) * wgt, __uint_as_float(v[c + 3]) * wgt);
+                for (int w = 16; w >= 1; w >>= 1) v += __shfl_xor_sync(FULL_MASK, v, w);
+                if (lane == c) l = v;
             }
+            lsum[q4 * NR + 32 * hh + lane] = l;
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(NMW * 32) : "memory");
-        if (is_row) {
-            // dims [32 (2 ch + sub), + 32) of the row: the sum of its two lanes in both chains
-            const bool failed = *bad != 0 || *abort_flag != 0;
-            const int d0 = 32 * (2 * ch + sub);
-            const int la = ml & ~16, lb = ml | 16;
-            float4* o = reinterpret_cast<float4*>(out_row(row) + d0);
+        asm volatile("bar.sync 3, %0;" ::"r"(NMW * 32) : "memory");
+        const bool failed = *bad != 0 || *abort_flag != 0;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int half = 0; half < 2; ++half) {  // 16 rows at a time
+            uint32_t ohi[16], olo[16];
+            tmem_ld_x16(tl + TO + uint32_t(32 * hh + 16 * half), ohi);
+            tmem_ld_x16(tl + TO + uint32_t(64 + 32 * hh + 16 * half), olo);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float4 v = *reinterpret_cast<const float4*>(opart + (size_t(k >> 1) * 128 + ((k & 1) ? lb : la)) * D + d0 + 4 * c);
-                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            for (int c = 0; c < 16; ++c) {
+                const int r = 32 * hh + 16 * half + c;
+                if (r < RR) {
+                    const float l = lsum[r] + lsum[NR + r] + lsum[2 * NR + r] + lsum[3 * NR + r];
+                    const float inv = l == 0.f ? 0.f : 1.f / l;  // no token: 0; a NaN input stays NaN
+                    const float o = nt == 0 ? 0.f : (__uint_as_float(ohi[c]) + __uint_as_float(olo[c])) * inv;
+                    out_row(r)[tk] = failed ? NAN : o;
                 }
-                o[c] = failed ? make_float4(NAN, NAN, NAN, NAN) : acc;
             }
         }
     }
@@ -1467,6 +1544,8 @@ static pf_status multi_query_setup(const void* q, const void* k_cache, const voi
     MultiParams& p = *pp;
     p = MultiParams{};
     p.q = static_cast<const uint16_t*>(q);
+    p.k_cache = static_cast<const uint16_t*>(k_cache);
+    p.v_cache = static_cast<const uint16_t*>(v_cache);
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.out = out;
