@@ -900,8 +900,8 @@ __global__ void __launch_bounds__((MT * NG + NPW) * 32, 2) paged_multi_query_wid
 //    (a shuffle transpose and shared memory), move the references and rescale those rows
 //    of O^T in place once the previous product is complete.  Each thread writes its
 //    token's P row into P^T (swizzled, MN-major) and keeps the row sums of its tokens;
-//    at the end they are summed over the tile's lanes and O^T is read, normalised and
-//    written out row by row (a warp writes 32 consecutive dimensions).
+//    at the end they are summed over the tile's lanes (a transposed shuffle) and O^T is
+//    staged through P^T's buffer, so that each warp writes 8 whole normalised output rows.
 // Every wait is bounded; one that gives up raises an abort flag that ends the others at
 // once, and every role still runs all its iterations, so the CTA stays in step and
 // releases its tensor memory.
@@ -947,6 +947,22 @@ struct TcLayout {
 // Starts pulling `bytes` (a multiple of 16) of global memory at `src` (16-byte aligned) into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Sum over the warp's 32 lanes of each of 32 values, transposed: lane l returns the sum
+// of value l (31 shuffles instead of 160).  The values are consumed.
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane) {
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool up = (lane & w) != 0;
+#pragma unroll
+        for (int c = 0; c < w; ++c) {
+            const float send = up ? v[c] : v[c + w];
+            const float keep = up ? v[c + w] : v[c];
+            v[c] = keep + __shfl_xor_sync(FULL_MASK, send, w);
+        }
+    }
+    return v[0];
 }
 
 // fp32 <-> int32 keys whose signed order is the order of the floats (-inf lowest), for
@@ -1361,38 +1377,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
             if (lane == 0) mbar_arrive(bar(PFULL));
         }
 
-        // ---- epilogue: all MMAs are done; row sums over the tile's 128 token lanes, then O^T row by row
+        // ---- epilogue.  Row sums over the tile's 128 token lanes (lane c of each warp: row
+        // 32 hh + c) while the last products run; then, once every MMA is complete, each half's
+        // O^T block goes through P^T's buffer (no product reads it any more) so that a warp
+        // writes 8 whole output rows with 16-byte stores
+        lsum[q4 * NR + 32 * hh + lane] = warp_transpose_sum(l_part, lane);
         wait(DONE, 0);
         __syncwarp();
         tc_fence_after_sync();
-        {
-            float l = 0.f;  // lane c: row 32 hh + c
+        float* blk = reinterpret_cast<float*>(smem + Lay::PT) + hh * 32 * D;  // [32 rows][D] fp32 of this half
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                float v = l_part[c];
-#pragma unroll
-                for (int w = 16; w >= 1; w >>= 1) v += __shfl_xor_sync(FULL_MASK, v, w);
-                if (lane == c) l = v;
-            }
-            lsum[q4 * NR + 32 * hh + lane] = l;
-        }
-        asm volatile("bar.sync 3, %0;" ::"r"(NMW * 32) : "memory");
-        const bool failed = *bad != 0 || *abort_flag != 0;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {  // 16 rows at a time
+        for (int half = 0; half < 2; ++half) {  // 16 rows at a time: dim tk of rows 32 hh + 16 half + c
             uint32_t ohi[16], olo[16];
             tmem_ld_x16(tl + TO + uint32_t(32 * hh + 16 * half), ohi);
             tmem_ld_x16(tl + TO + uint32_t(64 + 32 * hh + 16 * half), olo);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const int r = 32 * hh + 16 * half + c;
-                if (r < RR) {
-                    const float l = lsum[r] + lsum[NR + r] + lsum[2 * NR + r] + lsum[3 * NR + r];
-                    const float inv = l == 0.f ? 0.f : 1.f / l;  // no token: 0; a NaN input stays NaN
-                    const float o = nt == 0 ? 0.f : (__uint_as_float(ohi[c]) + __uint_as_float(olo[c])) * inv;
-                    out_row(r)[tk] = failed ? NAN : o;
-                }
-            }
+            for (int c = 0; c < 16; ++c)
+                blk[(16 * half + c) * D + tk] = __uint_as_float(ohi[c]) + __uint_as_float(olo[c]);
+        }
+        asm volatile("bar.sync 3, %0;" ::"r"(NMW * 32) : "memory");
+        const bool failed = *bad != 0 || *abort_flag != 0;
+#pragma unroll 2
+        for (int i = 0; i < 8; ++i) {  // rows 32 hh + 8 q4 + i; lane l: dims 4 l .. 4 l + 3
+            const int rl = 8 * q4 + i, r = 32 * hh + rl;
+            if (r >= RR) break;
+            const float l = lsum[r] + lsum[NR + r] + lsum[2 * NR + r] + lsum[3 * NR + r];
+            const float inv = l == 0.f ? 0.f : 1.f / l;  // no token: 0; a NaN input stays NaN
+            const float4 v = *reinterpret_cast<const float4*>(blk + rl * D + 4 * lane);
+            float4 o = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+            if (nt == 0) o = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (failed) o = make_float4(NAN, NAN, NAN, NAN);
+            *reinterpret_cast<float4*>(out_row(r) + 4 * lane) = o;
         }
     }
 
