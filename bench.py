@@ -321,7 +321,7 @@ class MultiQueryRunner:
     """pf_paged_attention_multi_query over a resident workload: the last q_len tokens of
     every sequence are its new tokens (draft tokens under verification)."""
 
-    def __init__(self, pf, runner, q_len, kernel="mma"):
+    def __init__(self, pf, runner, q_len, kernel="auto"):
         import torch
         from workloads import multi_query
         self.pf, self.r, self.q_len, self.kernel = pf, runner, q_len, kernel
@@ -526,9 +526,9 @@ def main():
     extras = {}
     if not args.no_extras and rank == 0:
         g = wl.num_q_heads // wl.num_kv_heads
-        runs = [(q_len, "mma") for q_len in (4, 8, 12, 16)]
+        runs = [(q_len, "auto") for q_len in (4, 8, 12, 16)]
         if wl.head_dim == 128:
-            runs += [(8, "tcgen05"), (16, "tcgen05")]
+            runs += [(8, "tcgen05")]  # past 32 rows the default entry runs the tcgen05 kernel itself
         for q_len, kernel in runs:
             if runner.split or g * q_len > 64:
                 continue

@@ -181,11 +181,12 @@ PF_API pf_status pf_paged_attention_decode_append(const void* q, const void* k_n
  * replaced); a NaN or infinite *value* there may make the row NaN, since the
  * tensor-core P.V product multiplies it by the row's zero probability.  Finite
  * caches are unaffected.  The scores and P.V
- * run on tensor cores (mma.sync, bf16 inputs, fp32 accumulation; the
- * probabilities enter P.V as a bf16 high part plus a bf16 remainder).  Up to 16
- * rows per kv head (g * q_len) one CTA's four warps split the tokens; from 17 to
- * 64 rows each 16-row tile has its own warp and one or two producer warps stream K/V to
- * all of them.
+ * run on tensor cores (bf16 inputs, fp32 accumulation; the probabilities enter
+ * P.V as a bf16 high part plus a bf16 remainder).  By rows per kv head
+ * (g * q_len): up to 16, one CTA's four warps split the tokens (mma.sync); 17 to
+ * 32, and 33 to 64 at head_dim 64, each 16-row tile has its own warp and one or
+ * two producer warps stream K/V to all of them (mma.sync); 33 to 64 at head_dim
+ * 128 run the kernel of pf_paged_attention_multi_query_tcgen05.
  *
  *   q    [num_seqs, q_len, num_q_heads, head_dim] bf16, 16-byte aligned
  *   out  [num_seqs, q_len, num_q_heads, head_dim] fp32
@@ -202,16 +203,17 @@ PF_API pf_status pf_paged_attention_multi_query(const void* q, const void* k_cac
 /*
  * The same operation as pf_paged_attention_multi_query, with both products on
  * the fifth-generation tensor cores (tcgen05.mma, accumulators in tensor
- * memory): per (sequence, kv head) one CTA streams K/V tiles of 64 tokens; the
- * scores S = Q K^T (query rows from tensor memory) and O = P V (probabilities,
- * as bf16 high part plus remainder, from tensor memory) are single-CTA MMAs
- * whose operands the TMA copies straight from the cache blocks.  Results agree
- * with pf_paged_attention_multi_query to fp32 rounding.  On the Llama-3-8B-
- * shaped batch it is slower than that kernel at every row count (about 1.3 ms
- * against 0.83-1.21 ms at 32-64 rows): per 64-token tile a CTA runs a chain of
- * ~16 MMAs from one issuing thread and a softmax, two such chains interleaved,
- * and a lone CTA is no faster than one in a full GPU.  It is the tensor-memory
- * formulation of the step, kept as an alternative.
+ * memory), computed transposed so that a tile's 128 tokens (and the 128 head
+ * dimensions) fill the MMA's 128 lanes and the query rows are its N side:
+ * S^T = K Q^T, then O^T += V^T P^T with P as bf16 high part plus remainder.
+ * One CTA per (sequence, kv head) streams 128-token K and V tiles (TMA copies of
+ * the cache blocks, three- and two-deep rings) straight into the swizzled
+ * operand layout.  Results agree with the mma.sync kernels to fp32 rounding.
+ * pf_paged_attention_multi_query runs it for 33-64 rows at head_dim 128, where
+ * it is the faster one (Llama-3-8B-shaped batch: 886 and 905 us at 48 and 64
+ * rows against 1,148 and 1,211 us); at 32 rows and below the mma.sync kernels
+ * are faster (827 against 864 us at 32 rows), since a 128-token tile's products
+ * cost the same whatever the row count.
  *
  * Supported: head_dim == 128 (else PF_ERR_UNSUPPORTED); the other shapes,
  * arguments and errors as pf_paged_attention_multi_query.

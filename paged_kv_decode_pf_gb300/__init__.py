@@ -210,11 +210,12 @@ def paged_attention_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: t
 def paged_attention_multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                                 block_tables: torch.Tensor, context_lens: torch.Tensor,
                                 scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                                kernel: str = "mma") -> torch.Tensor:
+                                kernel: str = "auto") -> torch.Tensor:
     """q [S, q_len, Hq, D]: the last q_len tokens of each sequence, already in the cache, attend causally.
-    Returns out [S, q_len, Hq, D] fp32.  Needs (Hq / Hkv) * q_len <= 64.  kernel="tcgen05" runs
-    pf_paged_attention_multi_query_tcgen05 (D = 128 only) instead of pf_paged_attention_multi_query."""
-    if kernel not in ("mma", "tcgen05"):
+    Returns out [S, q_len, Hq, D] fp32.  Needs (Hq / Hkv) * q_len <= 64.  kernel="auto" calls
+    pf_paged_attention_multi_query (which picks its kernel by row count); kernel="tcgen05" calls
+    pf_paged_attention_multi_query_tcgen05 (D = 128 only)."""
+    if kernel not in ("auto", "tcgen05"):
         raise ValueError(f"paged_attention_multi_query: unknown kernel {kernel!r}")
     _cuda(q, "q", _BF16, 4)
     _cuda(k_cache, "k_cache", _BF16, 4)

@@ -1518,12 +1518,14 @@ template <int D>
 static cudaError_t launch_multi_any(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p,
                                     cudaStream_t stream) {
     if (p.rows <= kMultiMaxRows) return launch_multi<D>(mk, mv, p, stream);
-    switch ((p.rows + 15) / 16) {
-        // producer warps: two where the consumers' registers allow (the 32-row variant), else one
-        case 2: return launch_multi_wide<D, 2, 2, PF_WIDE_NST_2, PF_WIDE_OPT_2, 2>(mk, mv, p, stream);  // two groups
-        case 3: return launch_multi_wide<D, 3, 1, PF_WIDE_NST_3, PF_WIDE_OPT_3, 1>(mk, mv, p, stream);
-        default: return launch_multi_wide<D, 4, 1, PF_WIDE_NST_4, PF_WIDE_OPT_4, 1>(mk, mv, p, stream);
+    // producer warps: two where the consumers' registers allow (the 32-row variant), else one.
+    // At D = 128 rows past 32 go to the tcgen05 kernel instead.
+    if (p.rows <= 32) return launch_multi_wide<D, 2, 2, PF_WIDE_NST_2, PF_WIDE_OPT_2, 2>(mk, mv, p, stream);  // two groups
+    if constexpr (D == 64) {
+        if (p.rows <= 48) return launch_multi_wide<D, 3, 1, PF_WIDE_NST_3, PF_WIDE_OPT_3, 1>(mk, mv, p, stream);
+        return launch_multi_wide<D, 4, 1, PF_WIDE_NST_4, PF_WIDE_OPT_4, 1>(mk, mv, p, stream);
     }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pf
@@ -1593,8 +1595,14 @@ extern "C" pf_status pf_paged_attention_multi_query(const void* q, const void* k
                                            num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                                            num_blocks, scale, out, &mk, &mv, &p);
     if (st != PF_OK || num_seqs == 0) return st;
-    const cudaError_t e = head_dim == 64 ? launch_multi_any<64>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream))
-                                         : launch_multi_any<128>(mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (head_dim == 64)
+        e = launch_multi_any<64>(mk, mv, p, s);
+    else if (p.rows <= 32)
+        e = launch_multi_any<128>(mk, mv, p, s);
+    else
+        e = launch_multi_tc(mk, mv, p, s);  // 33 to 64 rows at D = 128: the tcgen05 kernel
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }
 

@@ -57,7 +57,7 @@ def test_random_shapes(pf, oracle_lib, seed):
     q = multi_query(wl, q_len)
     qt = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).view(torch.bfloat16).cuda()
     mq_ref = oracle_lib.paged_attention_multi(q, kc, vc, wl.block_tables, wl.context_lens, wl.scale)
-    for kernel in ("mma", "tcgen05") if wl.head_dim == 128 else ("mma",):
+    for kernel in ("auto", "tcgen05") if wl.head_dim == 128 else ("auto",):
         mq = pf.paged_attention_multi_query(qt, d["k_cache"], d["v_cache"], d["block_tables"],
                                             d["context_lens"], kernel=kernel).cpu().numpy()
         assert pf.get_device_error() == pf.PF_OK

@@ -55,7 +55,7 @@ def test_multi_query_in_a_graph(pf):
     wl = make_workload("graphmq", 4, 32, 8, 128, 16, [40, 100, 260, 33], seed=92, pool_scale=2)
     d = to_device(wl)
     # the 16-row kernel, the wide one and the tcgen05 form
-    for q_len, kernel in ((4, "mma"), (8, "mma"), (8, "tcgen05")):
+    for q_len, kernel in ((4, "auto"), (8, "auto"), (8, "tcgen05")):
         qt = torch.from_numpy(np.ascontiguousarray(multi_query(wl, q_len)).view(np.int16)).view(
             torch.bfloat16).cuda()
         out = torch.empty((wl.num_seqs, q_len, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device="cuda")

@@ -1,5 +1,5 @@
-"""Multi-token paged query (pf_paged_attention_multi_query and its tcgen05 form,
-pf_paged_attention_multi_query_tcgen05) on the GPU against the oracle.
+"""Multi-token paged query (pf_paged_attention_multi_query, which picks its kernel by row count,
+and pf_paged_attention_multi_query_tcgen05) on the GPU against the oracle.
 
 The last q_len tokens of every sequence are the new ones (already in the cache);
 row (j, h) attends causally to the tokens t <= L - q_len + j."""
@@ -13,7 +13,7 @@ from workloads import BF16_NAN, make_workload, multi_query
 pytestmark = pytest.mark.gpu
 
 
-def run_multi(pf, d, q, kernel="mma"):
+def run_multi(pf, d, q, kernel="auto"):
     qt = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).view(torch.bfloat16).cuda()
     out = pf.paged_attention_multi_query(qt, d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
                                          kernel=kernel)
@@ -31,7 +31,7 @@ CASES = [
     (16, 4, 64, 16, 6), (8, 8, 64, 32, 20),                            # 24 and 20 rows at D=64 (two groups)
 ]
 # the tcgen05 form is D = 128 only
-KERNEL_CASES = [c + ("mma",) for c in CASES] + [c + ("tcgen05",) for c in CASES if c[2] == 128]
+KERNEL_CASES = [c + ("auto",) for c in CASES] + [c + ("tcgen05",) for c in CASES if c[2] == 128]
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,bs,Q,kernel", KERNEL_CASES)
@@ -52,7 +52,7 @@ def test_multi_query_single_token_matches_decode(pf):
     check_close(got, dec.cpu().numpy(), abs_tol=2e-5, rel_tol=1e-4)
 
 
-@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
+@pytest.mark.parametrize("kernel", ["auto", "tcgen05"])
 def test_multi_query_llama3_shaped_batch(pf, oracle_lib, kernel):
     """64 sequences, 32 q / 8 kv heads, 4 draft tokens: every row against the oracle."""
     wl = make_workload("mq64", 64, 32, 8, 128, 16, ("uniform", 1024, 4096), seed=102)
@@ -62,7 +62,7 @@ def test_multi_query_llama3_shaped_batch(pf, oracle_lib, kernel):
     check_close(got, ref)
 
 
-@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
+@pytest.mark.parametrize("kernel", ["auto", "tcgen05"])
 def test_multi_query_wide_llama3_shaped_batch(pf, oracle_lib, kernel):
     """64 sequences, 32 q / 8 kv heads, 16 draft tokens (64 rows per kv head): every row."""
     wl = make_workload("mq64w", 64, 32, 8, 128, 16, ("uniform", 1024, 4096), seed=104)
@@ -72,7 +72,7 @@ def test_multi_query_wide_llama3_shaped_batch(pf, oracle_lib, kernel):
     check_close(got, ref)
 
 
-@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
+@pytest.mark.parametrize("kernel", ["auto", "tcgen05"])
 def test_multi_query_wide_bad_block_and_length(pf, oracle_lib, kernel):
     """32 rows per kv head meet a table entry outside the pool and a length beyond the table:
     those sequences' rows are NaN, the others match the oracle, and the word is set."""
@@ -99,10 +99,11 @@ def test_multi_query_rows_beyond_sixty_four_are_unsupported(pf):
     assert e.value.status == pf.PF_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("q_len,kernel", [(4, "mma"), (16, "mma"), (16, "tcgen05")])
+@pytest.mark.parametrize("q_len,kernel", [(4, "auto"), (8, "auto"), (16, "auto")])
 def test_multi_query_llama3_full_size(pf, oracle_lib, config_workload, q_len, kernel):
-    """The launches the bench times: all 256 Llama-3-shaped sequences (4.8 GB of K/V) with 4
-    and with 16 draft tokens (16 and 64 query rows per kv head), every row against the oracle."""
+    """The launches the bench times: all 256 Llama-3-shaped sequences (4.8 GB of K/V) with 4, 8
+    and 16 draft tokens (16, 32 and 64 query rows per kv head: the three kernels the default
+    entry picks), every row against the oracle."""
     wl = config_workload(4)
     q = multi_query(wl, q_len)
     got = run_multi(pf, to_device(wl), q, kernel)
@@ -111,7 +112,7 @@ def test_multi_query_llama3_full_size(pf, oracle_lib, config_workload, q_len, ke
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
+@pytest.mark.parametrize("kernel", ["auto", "tcgen05"])
 def test_multi_query_poisoned_new_token(pf, kernel):
     """A NaN key at the third new token of one sequence reaches exactly the rows whose causal
     window holds it: new tokens 2 .. q_len-1 of that kv head's query heads (the masked scores of
@@ -141,14 +142,25 @@ def test_multi_query_poisoned_new_token(pf, kernel):
             assert bad[expect].all() and not bad[~group].any()
 
 
-def test_multi_query_tcgen05_agrees_with_mma(pf):
-    """The two formulations of the step agree to fp32 rounding at every row count up to 64."""
+def test_multi_query_tcgen05_agrees_with_mma_sync(pf):
+    """The tcgen05 kernel and the mma.sync kernels the default entry runs up to 32 rows per kv head
+    agree to fp32 rounding at every such row count."""
     wl = make_workload("mqagree", 8, 32, 8, 128, 16, ("uniform", 1, 900), seed=108, pool_scale=2)
     d = to_device(wl)
-    for Q in (1, 3, 4, 5, 8, 11, 16):
+    for Q in (1, 3, 4, 5, 8):
         q = multi_query(wl, Q)
-        a, b = run_multi(pf, d, q, "mma"), run_multi(pf, d, q, "tcgen05")
+        a, b = run_multi(pf, d, q, "auto"), run_multi(pf, d, q, "tcgen05")
         assert np.abs(a - b).max() <= 2e-5, Q
+
+
+def test_multi_query_default_runs_tcgen05_past_32_rows(pf):
+    """At head_dim 128 the default entry serves 33 to 64 rows per kv head with the tcgen05 kernel:
+    its outputs are those of the explicit entry, bit for bit."""
+    wl = make_workload("mqdisp", 8, 32, 8, 128, 16, ("uniform", 1, 900), seed=111, pool_scale=2)
+    d = to_device(wl)
+    for Q in (9, 12, 16):
+        q = multi_query(wl, Q)
+        assert np.array_equal(run_multi(pf, d, q, "auto"), run_multi(pf, d, q, "tcgen05")), Q
 
 
 def test_multi_query_tcgen05_is_d128_only(pf):
