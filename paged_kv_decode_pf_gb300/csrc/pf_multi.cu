@@ -43,8 +43,6 @@ constexpr int kMultiMaxRows = 16;  // g * q_len: one m16 tile of query rows
 
 struct MultiParams {
     const uint16_t* q;          // [S, q_len, Hq, D]
-    const uint16_t* k_cache;    // [NB, Hkv, bs, D] (L2 prefetches; the copies go through the tensor maps)
-    const uint16_t* v_cache;
     const int32_t* block_tables;
     const int32_t* context_lens;
     float* out;                 // [S, q_len, Hq, D]
@@ -905,22 +903,11 @@ __global__ void __launch_bounds__((MT * NG + NPW) * 32, 2) paged_multi_query_wid
 // Every wait is bounded; one that gives up raises an abort flag that ends the others at
 // once, and every role still runs all its iterations, so the CTA stays in step and
 // releases its tensor memory.
-#ifndef PF_TC_KSTAGES
-#define PF_TC_KSTAGES 3
-#endif
-#ifndef PF_TC_VSTAGES
-#define PF_TC_VSTAGES 2
-#endif
-#ifndef PF_TC_PREFETCH
-#define PF_TC_PREFETCH 0
-#endif
 constexpr int kTcTok = 128;       // tokens per tile
-constexpr int kTcKStages = PF_TC_KSTAGES;  // K ring depth
-constexpr int kTcVStages = PF_TC_VSTAGES;  // V ring depth
-constexpr int kTcPrefetch = PF_TC_PREFETCH;  // tiles ahead of the copies whose blocks are prefetched into L2 (0: none)
+constexpr int kTcKStages = 3;     // K ring depth
+constexpr int kTcVStages = 2;     // V ring depth
 constexpr int kTcRows = 64;       // query rows per kv head (the N of the score product)
 constexpr int kTcCols = 256;      // TMEM columns: score buffers [0, 64) and [64, 128), O^T [128, 256)
-static_assert(kTcPrefetch >= 0 && kTcPrefetch <= 4, "prefetched tiles lie in the current or the next table batch");
 constexpr int kTcProducers = 4;   // issuing warps: two for K, two for V
 constexpr int kTcMath = 8;        // softmax warps
 constexpr int kTcThreads = 32 * (kTcProducers + 1 + kTcMath);
@@ -943,11 +930,6 @@ struct TcLayout {
     static constexpr int BYTES = MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;                         // room to align to 1024
 };
-
-// Starts pulling `bytes` (a multiple of 16) of global memory at `src` (16-byte aligned) into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 // Sum over the warp's 32 lanes of each of 32 values, transposed: lane l returns the sum
 // of value l (31 shuffles instead of 160).  The values are consumed.
@@ -1085,18 +1067,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
             int e[BOXES / 2];
 #pragma unroll
             for (int i = 0; i < BOXES / 2; ++i) e[i] = __shfl_sync(FULL_MASK, ent_cur, (j % TPB) * BOXES + pw + 2 * i);
-            if (kTcPrefetch > 0 && pw == 0 && j + kTcPrefetch < nt) {
-                // lanes 0-7 of the first warp of each tensor start tile j + kTcPrefetch's boxes toward L2,
-                // so that the ring's copies find them there; its entries are in this batch or the next
-                const int jt = j + kTcPrefetch, src = (jt % TPB) * BOXES + (lane & (BOXES - 1));
-                const int ec = __shfl_sync(FULL_MASK, ent_cur, src), en = __shfl_sync(FULL_MASK, ent_nxt, src);
-                const int ef = jt / TPB == j / TPB ? ec : en;
-                const int tok = jt * TOK + (lane & (BOXES - 1)) * kTileTokens;
-                if (lane < BOXES && tok < L && ef >= 0 && (long long)ef < p.num_blocks)
-                    bulk_prefetch_l2((is_v ? p.v_cache : p.k_cache) +
-                                         ((size_t(ef) * Hkv + kvh) * bs + block_offset(tok)) * D,
-                                     kTileTokens * D * 2);
-            }
             const int s = j % NS;
             bool ok = true;
             if (lane == 0 && j >= NS) ok = wait(EMPTYB + s, ((j / NS) - 1) & 1);
@@ -1561,8 +1531,6 @@ static pf_status multi_query_setup(const void* q, const void* k_cache, const voi
     MultiParams& p = *pp;
     p = MultiParams{};
     p.q = static_cast<const uint16_t*>(q);
-    p.k_cache = static_cast<const uint16_t*>(k_cache);
-    p.v_cache = static_cast<const uint16_t*>(v_cache);
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.out = out;
