@@ -185,3 +185,17 @@ def test_multi_query_two_groups_repeated(pf):
     outs = [pf.paged_attention_multi_query(*args) for _ in range(200)]
     assert pf.get_device_error() == pf.PF_OK
     assert all(torch.equal(o, first) for o in outs)
+
+
+def test_multi_query_tcgen05_repeated(pf):
+    """64 rows per kv head through the tcgen05 kernel (the default entry's choice there): 100
+    launches back to back give bit-identical outputs and leave the error word clear (a role that
+    read a stage, a score buffer or P^T out of turn would change a result or stall)."""
+    wl = make_workload("mqrep_tc", 64, 32, 8, 128, 16, ("uniform", 1, 3000), seed=112)
+    d = to_device(wl)
+    qt = torch.from_numpy(np.ascontiguousarray(multi_query(wl, 16)).view(np.int16)).view(torch.bfloat16).cuda()
+    args = (qt, d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"])
+    first = pf.paged_attention_multi_query(*args)
+    outs = [pf.paged_attention_multi_query(*args) for _ in range(100)]
+    assert pf.get_device_error() == pf.PF_OK
+    assert all(torch.equal(o, first) for o in outs)
