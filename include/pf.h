@@ -311,7 +311,7 @@ PF_API pf_status pf_get_device_error(pf_stream_t stream);
 PF_API const char* pf_status_string(pf_status status);
 
 /*
- * Failure-detection check (not part of the paper's method): launches one
+ * Failure-detection check (not part of the attention method): launches one
  * block whose thread waits on a shared-memory barrier that nothing completes,
  * through the same bounded wait the attention kernels use, giving up after
  * about limit_ns nanoseconds (1e3 .. 1e10).  The kernel then returns normally,
@@ -321,7 +321,7 @@ PF_API const char* pf_status_string(pf_status status);
 PF_API pf_status pf_debug_bounded_wait(int64_t limit_ns, pf_stream_t stream);
 
 /*
- * Split-K decode that allocates nothing.  The paper has no counterpart; this
+ * Split-K decode that allocates nothing.  The source pages have no counterpart; this
  * exists for callers that cannot hand the library a workspace: a plugin or
  * custom op inside a host runtime that owns all device memory and offers no
  * allocator on the decode path, a decode loop that must not call cudaMalloc
