@@ -1195,16 +1195,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
         const uint32_t tl = tmem + (uint32_t(q4 * 32) << 16);  // this warp's TMEM lane quarter
         const int barid = 1 + hh;                              // named barrier of the row half's four warps
 
-        // Q (rows past RR zero) into its swizzled K-major tile: 1024 chunks of 16 bytes
-        for (int i = mw * 32 + lane; i < NR * 16; i += NMW * 32) {
-            const int r = i >> 4, c16 = i & 15;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < RR) {
-                const int j = r / G, h = r - (r / G) * G;
-                v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D) + c16);
+        // Q (rows past RR zero) into its swizzled K-major tile: 1024 chunks of 16 bytes, four per
+        // thread, all loads in flight before the first store
+        {
+            constexpr int PER = NR * 16 / (NMW * 32);
+            uint4 v[PER];
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int i = mw * 32 + lane + k * NMW * 32, r = i >> 4, c16 = i & 15;
+                v[k] = make_uint4(0, 0, 0, 0);
+                if (r < RR) {
+                    const int j = r / G, h = r - (r / G) * G;
+                    v[k] = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D) + c16);
+                }
             }
-            *reinterpret_cast<uint4*>(smem + Lay::QS + (c16 >> 3) * (NR * 128) + r * 128 +
-                                      (((c16 & 7) ^ (r & 7)) << 4)) = v;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int i = mw * 32 + lane + k * NMW * 32, r = i >> 4, c16 = i & 15;
+                *reinterpret_cast<uint4*>(smem + Lay::QS + (c16 >> 3) * (NR * 128) + r * 128 +
+                                          (((c16 & 7) ^ (r & 7)) << 4)) = v[k];
+            }
         }
         fence_proxy_async_smem();
         __syncwarp();
