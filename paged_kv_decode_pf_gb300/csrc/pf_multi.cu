@@ -883,10 +883,10 @@ __global__ void __launch_bounds__((MT * NG + NPW) * 32, 2) paged_multi_query_wid
 // (by its shared memory), 256 TMEM columns (two 64-column score buffers, O^T).
 //  * warps 0-1 stream the sequence's K tiles through a 3-deep ring and warps 2-3 its V
 //    tiles through a 2-deep one, each warp copying half of a tile's eight 16-token boxes
-//    (TMA tensor copies with the 128-byte swizzle, issued by lane 0); the blocks of a
-//    sequence lie anywhere in the pool and one thread's copies to scattered pages are
-//    served one after another, so four warps issue.  Table entries are fetched 32 boxes
-//    at a time, a batch ahead;
+//    (TMA tensor copies with the 128-byte swizzle, one per box and dim half, issued by
+//    eight lanes); the blocks of a sequence lie anywhere in the pool and one thread's
+//    copies to scattered pages are served one after another, so four warps issue.  Table
+//    entries are fetched 32 boxes at a time, a batch ahead;
 //  * warp 4, lane 0 issues S^T(j) once K(j) has landed and its score buffer (j % 2) is
 //    read, and O^T += V(j)^T P(j)^T once P(j) is written and V(j) has landed, the latter
 //    first; S^T(j + 1) thus runs while the softmax of tile j does;
@@ -1085,17 +1085,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) paged_multi_query_tc_kernel(
                     }
                     bytes += good[i] ? 2u * kTileTokens * 128u : 0u;
                 }
-                const uint32_t full = bar(FULLB + s);
-                mbar_arrive_expect_tx(full, bytes);
-#pragma unroll
-                for (int i = 0; i < BOXES / 2; ++i) {
-                    if (!good[i]) continue;
-                    const int b = pw + 2 * i, tok = j * TOK + b * kTileTokens;
-                    const int y = (e[i] * Hkv + kvh) * bs + block_offset(tok);
-                    const uint32_t at = ring + uint32_t(s * Lay::STAGE + b * kTileTokens * 128);
-                    tma_load_2d(at, map, 0, y, full, policy);
-                    tma_load_2d(at + Lay::HALF, map, 64, y, full, policy);
-                }
+                mbar_arrive_expect_tx(bar(FULLB + s), bytes);
+            }
+            {
+                // lanes 0-7 issue one copy each (box pw + 2 (lane / 2), dim half lane % 2), once lane 0
+                // has set the byte count: copies from different threads to scattered pages go out side
+                // by side rather than one after another
+                __syncwarp();
+                const int el = __shfl_sync(FULL_MASK, ent_cur, ((j % TPB) * BOXES + pw + 2 * (lane >> 1)) & 31);
+                const int b = pw + 2 * (lane >> 1), hf = lane & 1, tok = j * TOK + b * kTileTokens;
+                if (lane < BOXES && tok < L && el >= 0 && (long long)el < p.num_blocks)
+                    tma_load_2d(ring + uint32_t(s * Lay::STAGE + b * kTileTokens * 128 + hf * Lay::HALF), map,
+                                64 * hf, (el * Hkv + kvh) * bs + block_offset(tok), bar(FULLB + s), policy);
             }
             ++issued;
         }
