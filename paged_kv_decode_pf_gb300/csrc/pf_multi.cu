@@ -930,6 +930,9 @@ struct TcLayout {
     static constexpr int BYTES = MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;                         // room to align to 1024
 };
+// one CTA per SM: the dynamic part plus the longest-first ranking's static arrays fit in a
+// block's 227 KiB of shared memory
+static_assert(TcLayout::ALLOC + (kMultiSortMax + 4) * 4 <= 227 * 1024, "shared memory of the tcgen05 kernel");
 
 // Sum over the warp's 32 lanes of each of 32 values, transposed: lane l returns the sum
 // of value l (31 shuffles instead of 160).  The values are consumed.
