@@ -59,8 +59,6 @@ def _bind(lib):
     lib.oracle_reshape_and_cache.restype = i64
     lib.oracle_paged_attention.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, P, i32]
     lib.oracle_paged_attention.restype = None
-    lib.oracle_paged_attention_pairs.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, P, i32, P, i32]
-    lib.oracle_paged_attention_pairs.restype = None
     lib.oracle_paged_attention_partition.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64,
                                                      i32, i32, P, P, P, i32]
     lib.oracle_paged_attention_partition.restype = None
@@ -146,21 +144,6 @@ class Oracle:
         out = np.zeros((S, Q, Hq, D), dtype=np.float64)
         self.lib.oracle_paged_attention_multi(qp, kp, vp, bp, cp, S, Q, Hq, Hkv, D, bs, bt.shape[1], float(scale),
                                               out.ctypes.data, threads)
-        return out
-
-    def paged_attention_pairs(self, q, k_cache, v_cache, block_tables, context_lens, scale, pairs,
-                              threads: int = 0):
-        S, Hq, D = q.shape
-        NB, Hkv, bs, _ = k_cache.shape
-        pr, pp = _c(np.asarray(pairs).reshape(-1, 2), np.int32)
-        q, qp = _c(q, np.uint16)
-        kc, kp = _c(k_cache, np.uint16)
-        vc, vp = _c(v_cache, np.uint16)
-        bt, bp = _c(block_tables, np.int32)
-        cl, cp = _c(context_lens, np.int32)
-        out = np.zeros((pr.shape[0], D), dtype=np.float64)
-        self.lib.oracle_paged_attention_pairs(qp, kp, vp, bp, cp, Hq, Hkv, D, bs, bt.shape[1], float(scale),
-                                              pp, pr.shape[0], out.ctypes.data, threads)
         return out
 
     def partition(self, q, k_cache, v_cache, block_tables, context_lens, scale, partition_size,

@@ -26,13 +26,3 @@ def attention(q: Sequence[float], K: Sequence[Sequence[float]], V: Sequence[Sequ
     z = sum(e)
     return [sum(e[t] * V[t][c] for t in range(L)) / z for c in range(D)]
 
-
-def gqa_attention(q, K, V, scale, num_kv_heads):
-    """q [Hq][D]; K, V [L][Hkv][D]; query head h reads kv head h // (Hq // Hkv)."""
-    Hq = len(q)
-    g = Hq // num_kv_heads
-    out = []
-    for h in range(Hq):
-        kh = h // g
-        out.append(attention(q[h], [row[kh] for row in K], [row[kh] for row in V], scale))
-    return out

@@ -200,28 +200,6 @@ void oracle_paged_attention(const uint16_t* q, const uint16_t* k_cache, const ui
     }
 }
 
-/* Only the listed (seq, q_head) pairs: pairs[2j] = seq, pairs[2j+1] = head; out: [n, D]. */
-void oracle_paged_attention_pairs(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
-                                  const int32_t* block_tables, const int32_t* context_lens,
-                                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                                  int max_blocks_per_seq, double scale, const int32_t* pairs, int n,
-                                  double* out, int num_threads) {
-    problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_q_heads, num_kv_heads,
-                   head_dim, block_size, max_blocks_per_seq, scale};
-    set_threads(num_threads);
-#ifdef _OPENMP
-#pragma omp parallel for schedule(dynamic, 1)
-#endif
-    for (int j = 0; j < n; ++j) {
-        int i = pairs[2 * j], h = pairs[2 * j + 1];
-        int L = context_lens[i];
-        double* s = (double*)malloc(sizeof(double) * (L > 0 ? L : 1));
-        double m, l;
-        attend_range(&P, query_row(&P, i, h), i, kv_head_of(&P, h), 0, L, s, out + (size_t)j * head_dim, &m, &l);
-        free(s);
-    }
-}
-
 /* ------------------------------------------------- multi-token query rows */
 
 /* Several new tokens per sequence (a chunk of a long prompt interleaved with
