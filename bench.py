@@ -616,14 +616,12 @@ def main():
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "storage_dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_description(wl, args.workload), "num_seqs": wl.num_seqs,
-                       "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
-                       "block_size": wl.block_size, "total_tokens": int(wl.context_lens.astype(np.int64).sum()),
-                       "step": "pf_paged_attention_decode" if not runner_split(args, wl) else
-                       "pf_paged_attention_decode_partition + pf_paged_attention_merge",
-                       "algorithmic_bytes_per_step": step_bytes,
-                       "l2": "inputs larger than L2, no flush" if flush is None else "L2 flushed between steps",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": dict(workload_config(wl, args.workload),
+                           step="pf_paged_attention_decode" if not runner_split(args, wl) else
+                           "pf_paged_attention_decode_partition + pf_paged_attention_merge",
+                           algorithmic_bytes_per_step=step_bytes,
+                           l2="inputs larger than L2, no flush" if flush is None else "L2 flushed between steps",
+                           parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
             "seq_steps_per_s": round(world * wl.num_seqs / (ms_step * 1e-3), 1),
             "us_per_call": round(ms_step * 1e3, 2),
             "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
@@ -648,6 +646,13 @@ def main():
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def workload_config(wl, index):
+    """The workload's name and shape keys, the same in both arms' `config`."""
+    return {"workload": workload_description(wl, index), "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
+            "total_tokens": int(wl.context_lens.astype(np.int64).sum())}
 
 
 def first_sequences(wl, n):
@@ -712,7 +717,7 @@ def reference_arm(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
             "warmup": warmup, "ms_per_step": round(el * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_description(wl, args.workload), "sample": desc},
+            "config": dict(workload_config(wl, args.workload), sample=desc),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": orc.max_threads(), "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

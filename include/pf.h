@@ -36,6 +36,12 @@
  *   Streams    every call is asynchronous and stream-ordered on `stream`
  *              (a cudaStream_t; NULL is the legacy default stream).  Calls are
  *              thread-safe.  The current CUDA device must own all pointers.
+ *   Devices    the first call on a device looks up, with that device current,
+ *              the device addresses of the library's per-device variables (the
+ *              error word; the scratch of pf_paged_attention_split_noalloc) and
+ *              keeps them for the life of the process.  cudaDeviceReset after a
+ *              call of this library is therefore not supported: the module may
+ *              be loaded again at another address.
  *   Errors     problems visible on the host (null or misaligned pointers,
  *              non-positive sizes, overflowing sizes) return PF_ERR_INVALID_ARG
  *              and shapes outside the compiled set return PF_ERR_UNSUPPORTED,
@@ -228,6 +234,14 @@ PF_API pf_status pf_paged_attention_multi_query_tcgen05(const void* q, const voi
 /*
  * Split over context partitions ("flash-decoding") for long contexts.
  *
+ * Source: no passage of the source pages describes a split of one sequence's
+ * context; the pages stop at decode-only block-table attention with online
+ * softmax (ForgeLLM README, feature list).  The pair below is defined by the
+ * identity that makes it exact: the softmax over a sequence's tokens, split into
+ * disjoint partitions, equals the combination of each partition's normalised
+ * result o_k weighted by l_k exp(m_k - M) (the merge formula further down), so
+ * partition pass + merge compute the same attention as pf_paged_attention_decode.
+ *
  * The workspace holds, for NP = ceil(max_context_len / partition_size)
  * partitions, three fp32 arrays, each starting on a 256-byte boundary:
  *   tmp_out [num_seqs][num_q_heads][NP][head_dim]  o_k = sum e_t V_t / l_k
@@ -265,7 +279,8 @@ PF_API pf_status pf_paged_attention_decode_partition(const void* q, const void* 
                                               size_t workspace_bytes, pf_stream_t stream);
 
 /*
- * Log-sum-exp merge of the partitions written by the partition pass:
+ * Log-sum-exp merge of the partitions written by the partition pass (the
+ * identity stated above the workspace layout; no page passage defines it):
  *   M = max_k m_k,  w_k = l_k exp(m_k - M),  out = sum_k w_k o_k / sum_k w_k
  * over k < ceil(context_lens[i] / partition_size); zero rows for empty
  * sequences.  The arguments must match the partition pass that filled the

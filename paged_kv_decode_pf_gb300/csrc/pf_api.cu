@@ -336,6 +336,20 @@ static cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group,
     return head_dim == 64 ? launch_decode_d64(p, group, mode, stream) : launch_decode_d128(p, group, mode, stream);
 }
 
+pf_status check_split_arguments(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int max_blocks_per_seq, int64_t num_blocks, float scale, int partition_size,
+                                int max_context_len) {
+    const AttnArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, max_blocks_per_seq, num_blocks, scale};
+    pf_status st = check_attention(a);
+    if (st != PF_OK) return st;
+    if (partition_size <= 0 || max_context_len < 0) return PF_ERR_INVALID_ARG;
+    if (partition_size % kTileTokens != 0) return PF_ERR_UNSUPPORTED;
+    return PF_OK;
+}
+
 }  // namespace pf
 
 using namespace pf;
@@ -468,10 +482,10 @@ pf_status pf_paged_attention_decode_partition(const void* q, const void* k_cache
                                               void* workspace, size_t workspace_bytes, pf_stream_t stream) {
     const AttnArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
                      head_dim, block_size, max_blocks_per_seq, num_blocks, scale};
-    pf_status st = check_attention(a);
+    pf_status st = check_split_arguments(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                                         num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                                         partition_size, max_context_len);
     if (st != PF_OK) return st;
-    if (partition_size <= 0 || max_context_len < 0) return PF_ERR_INVALID_ARG;
-    if (partition_size % kTileTokens != 0) return PF_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PF_OK;
     size_t off_o = 0, off_m = 0, off_l = 0;
     const size_t need = pf_paged_attention_partition_workspace_layout(num_seqs, num_q_heads, head_dim,

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "pf.h"
+
 namespace pf {
 
 // Tokens per K/V tile that one bulk copy moves; block_size and the partition
@@ -65,6 +67,16 @@ constexpr int kMaxSortedSeqsPartition = 1024;  // the prefix scan costs O(S / th
 // and the current device's SM count; both defined in pf_api.cu.
 cudaError_t error_word(unsigned** out);
 cudaError_t sm_count(int* out);
+
+// Host-side checks shared by the partition pass and the split that allocates
+// nothing: the decode arguments (shapes, alignment, supported sizes) plus
+// partition_size and max_context_len.  Returns PF_OK or the status the entry
+// point reports; the workspace itself is not checked here.
+pf_status check_split_arguments(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int max_blocks_per_seq, int64_t num_blocks, float scale, int partition_size,
+                                int max_context_len);
 
 // Launch the decode kernel in one of the MODE_* modes for one head_dim.
 // Returns cudaSuccess or the launch error.

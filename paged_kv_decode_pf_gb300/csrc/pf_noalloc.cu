@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "pf.h"
+#include "pf_internal.h"
 
 namespace {
 
@@ -46,22 +47,26 @@ extern "C" pf_status pf_paged_attention_split_noalloc(const void* q, const void*
                                                       int head_dim, int block_size, int max_blocks_per_seq,
                                                       int64_t num_blocks, float scale, int partition_size,
                                                       int max_context_len, float* out, pf_stream_t stream) {
-    size_t need = 0;
-    if (num_seqs > 0) {
-        need = pf_paged_attention_partition_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,
-                                                           partition_size);
-        if (need == 0) return PF_ERR_INVALID_ARG;
-        if (need > PF_SPLIT_NOALLOC_SCRATCH_BYTES) return PF_ERR_UNSUPPORTED;
-    }
+    // The same argument checks as the partition pass, so a bad argument is reported
+    // as such whatever the size; only then the size of the partials against the scratch.
+    pf_status st = pf::check_split_arguments(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                             num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                             num_blocks, scale, partition_size, max_context_len);
+    if (st != PF_OK) return st;
+    if (num_seqs == 0) return PF_OK;
+    if (out == nullptr || reinterpret_cast<uintptr_t>(out) % 16 != 0) return PF_ERR_INVALID_ARG;
+    const size_t need = pf_paged_attention_partition_workspace_size(num_seqs, num_q_heads, head_dim,
+                                                                    max_context_len, partition_size);
+    if (need == 0) return PF_ERR_INVALID_ARG;
+    if (need > PF_SPLIT_NOALLOC_SCRATCH_BYTES) return PF_ERR_UNSUPPORTED;
     void* scratch = nullptr;
-    if (num_seqs > 0 && scratch_address(&scratch) != cudaSuccess) return PF_ERR_CUDA;
+    if (scratch_address(&scratch) != cudaSuccess) return PF_ERR_CUDA;
     // Every partial the merge reads (partitions below ceil(L / P)) is written by the
     // partition pass of this same call, so the scratch needs no clearing.
-    pf_status st = pf_paged_attention_decode_partition(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
-                                                       num_q_heads, num_kv_heads, head_dim, block_size,
-                                                       max_blocks_per_seq, num_blocks, scale, partition_size,
-                                                       max_context_len, scratch, PF_SPLIT_NOALLOC_SCRATCH_BYTES,
-                                                       stream);
+    st = pf_paged_attention_decode_partition(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                                             num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                             scale, partition_size, max_context_len, scratch,
+                                             PF_SPLIT_NOALLOC_SCRATCH_BYTES, stream);
     if (st != PF_OK) return st;
     return pf_paged_attention_merge(scratch, context_lens, num_seqs, num_q_heads, head_dim, partition_size,
                                     max_context_len, out, stream);
