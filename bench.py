@@ -75,6 +75,16 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_peak():
+    """Dense bf16 tensor peak for a kernel timed alone: MEASURED_PEAKS.json's burst figure."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured burst, MEASURED_PEAKS.json bf16_tflops"
+    except Exception:
+        return 1900.0, "fallback 1.9 PFLOP/s"
+
+
 def decode_source_sha() -> str:
     h = hashlib.sha256()
     for rel in DECODE_SOURCES:
@@ -529,8 +539,10 @@ def main():
         runs = [(q_len, "auto") for q_len in (4, 8, 12, 16)]
         if wl.head_dim == 128:
             runs += [(8, "tcgen05")]  # past 32 rows the default entry runs the tcgen05 kernel itself
+        runs += [(64, "auto"), (128, "auto")]  # prompt chunks: past 64 rows per kv head, the chunk kernel
+        bf16_peak = measured_bf16_peak()
         for q_len, kernel in runs:
-            if runner.split or g * q_len > 64:
+            if runner.split or g * q_len > 65536:
                 continue
             # the same resident cache, with the last q_len tokens of every sequence as new (draft) tokens
             mr = MultiQueryRunner(pf, runner, q_len, kernel)
@@ -539,14 +551,18 @@ def main():
             mb = mr.step_bytes()
             fl = mr.step_flops()
             name = "pf_paged_attention_multi_query" + ("_tcgen05" if kernel == "tcgen05" else "")
+            chunk = g * q_len > 64
             extras[CONFIGS[args.workload].name + f"_multi_query_q{q_len}" + ("_tcgen05" if kernel == "tcgen05" else "")] = {
                 "description": f"{name} on the same cache: {q_len} new tokens per "
-                               f"sequence, causal among them ({g * q_len} query rows per kv head)",
+                               f"sequence, causal among them ({g * q_len} query rows per kv head"
+                               + (", prompt-chunk kernel)" if chunk else ")"),
                 "step": "multi_query", "us_dominant_kernel": round(ms_d * 1e3, 2), "algorithmic_bytes": mb,
                 "gbs_dominant_kernel": round(mb / (ms_d * 1e-3) / 1e9, 1),
                 "pct_of_8tbs_dominant": round(100 * mb / (ms_d * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
                 "frac_of_measured_peak_dominant": round(mb / (ms_d * 1e-3) / 1e9 / peak, 3),
                 "tflops_dominant_kernel": round(fl / (ms_d * 1e-3) / 1e12, 1),
+                "frac_of_measured_bf16_peak": round(fl / (ms_d * 1e-3) / 1e12 / bf16_peak[0], 3),
+                "bf16_peak": f"{bf16_peak[0]} TFLOP/s ({bf16_peak[1]})",
                 "l2": "inputs larger than L2",
             }
             del mr

@@ -212,9 +212,10 @@ def paged_attention_multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
                                 scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                                 kernel: str = "auto") -> torch.Tensor:
     """q [S, q_len, Hq, D]: the last q_len tokens of each sequence, already in the cache, attend causally.
-    Returns out [S, q_len, Hq, D] fp32.  Needs (Hq / Hkv) * q_len <= 64.  kernel="auto" calls
-    pf_paged_attention_multi_query (which picks its kernel by row count); kernel="tcgen05" calls
-    pf_paged_attention_multi_query_tcgen05 (D = 128 only)."""
+    Returns out [S, q_len, Hq, D] fp32.  Needs (Hq / Hkv) * q_len <= 65536.  kernel="auto" calls
+    pf_paged_attention_multi_query (which picks its kernel by row count: past 64 rows per kv head
+    the prompt-chunk kernel); kernel="tcgen05" calls pf_paged_attention_multi_query_tcgen05
+    (D = 128 only)."""
     if kernel not in ("auto", "tcgen05"):
         raise ValueError(f"paged_attention_multi_query: unknown kernel {kernel!r}")
     _cuda(q, "q", _BF16, 4)

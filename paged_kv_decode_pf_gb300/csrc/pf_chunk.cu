@@ -1,0 +1,478 @@
+// Prompt-chunk query: the multi-token query of pf_paged_attention_multi_query for more
+// than 64 query rows per kv head.
+//
+// A long prompt is fed to the model in bounded chunks interleaved with decode (ForgeLLM
+// README: "long prompts are split into bounded chunks and interleaved with decode"): the
+// chunk's q_len tokens are already appended to the paged cache and each attends to every
+// earlier token and to the chunk's tokens up to itself.  With g query heads per kv head a
+// (sequence, kv head) has R = g * q_len query rows, so for chunks of tens to hundreds of
+// tokens both products are real matrix products and the step is bound by the tensor
+// cores rather than by HBM.  Here the query rows are the M side of single-CTA tcgen05.mma:
+//     S(j)  = Q K(j)^T        M = 128 rows, N = 128 tokens, K = D
+//     O    += P(j) V(j)       M = 128 rows, N = D,          K = 128 tokens
+// with Q and the K / V tiles in shared memory (TMA tiles with the 128-byte swizzle) and S,
+// P and O in tensor memory.  P enters the product as its bf16 high part and the bf16
+// remainder (two MMAs against the same V tile), so the probabilities keep about 16
+// significant bits, as in the other multi-token kernels.
+//
+// One CTA per (sequence, kv head, tile of 128 rows); the row tiles of one (sequence, kv
+// head) are consecutive in the grid so that they stream the same K/V tiles at about the
+// same time and all but the first read them from L2.  Seven warps:
+//  * warps 0-3 (the softmax warpgroup): thread 32 w + l holds query row 32 w + l of the
+//    tile, which is lane 32 w + l of tensor memory, so a row's maximum and sum never leave
+//    its thread.  Per tile it reads its 128 scores, masks the tokens its row may not see,
+//    and moves its reference maximum only when a score exceeds it by more than 2^8 (the
+//    rescale of its O row then happens once the previous P.V is complete); it writes its
+//    probabilities' hi and lo parts into tensor memory as the A operand of P.V;
+//  * warp 4 issues the MMAs from one lane: S(j + 1) into the second score buffer while the
+//    softmax works on S(j), and P(j) V(j) as soon as P(j) is written;
+//  * warp 5 copies K tiles into a ring of KST stages and warp 6 V tiles into one of VST: a
+//    tile is eight 16-token boxes, and each box and dim half is one TMA copy issued by its
+//    own lane (copies of one thread to scattered pages are served one after another).
+// Every wait is bounded; one that gives up raises an abort flag that ends the others, and
+// every role still runs to its end, so tensor memory is always released.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "pf.h"
+#include "pf_device.cuh"
+#include "pf_internal.h"
+#include "pf_multi.cuh"
+#include "pf_tcgen05.cuh"
+
+namespace pf {
+
+constexpr int kChTok = 128;        // tokens per K/V tile: the N of S, the K of P.V
+constexpr int kChRows = 128;       // query rows per CTA: the M of both products
+constexpr int kChMath = 4;         // softmax warps (warp w: TMEM lanes 32 w .. 32 w + 31)
+constexpr int kChMmaWarp = kChMath;
+constexpr int kChProducers = 2;    // one warp copies K, one copies V
+constexpr int kChThreads = 32 * (kChMath + 1 + kChProducers);
+constexpr float kChRescale = 8.f;  // the reference maximum moves when a score exceeds it by more (log2 units)
+// tensor memory columns: score buffers, P (hi, lo), O
+constexpr uint32_t kChTS0 = 0, kChTS1 = 128, kChTP = 256, kChTO = 384, kChCols = 512;
+
+template <int D>
+struct ChunkLayout {
+    static constexpr int HALVES = D / 64;              // 128-byte swizzle rows per token (or query) row
+    static constexpr int HALF = kChTok * 128;          // 128 rows of 128 bytes: 16 KiB
+    static constexpr int TILE = HALVES * HALF;         // the Q tile, or one K or V tile
+    static constexpr int KST = D == 128 ? 3 : 5;       // K ring depth
+    static constexpr int VST = D == 128 ? 2 : 4;       // V ring depth
+    static constexpr int QS = 0;
+    static constexpr int KRING = QS + TILE;
+    static constexpr int VRING = KRING + KST * TILE;
+    static constexpr int NBARS = 2 * KST + 2 * VST + 8;
+    static constexpr int BARS = VRING + VST * TILE;
+    static constexpr int MISC = BARS + ((NBARS * 8 + 15) / 16) * 16;  // TMEM base, bad-block flag, abort flag
+    static constexpr int BYTES = MISC + 16;
+    static constexpr int ALLOC = BYTES + 1024;  // room to align the operands to 1 KiB
+};
+static_assert(ChunkLayout<128>::ALLOC + (kMultiSortMax + 4) * 4 <= 227 * 1024, "shared memory, D = 128");
+static_assert(ChunkLayout<64>::ALLOC + (kMultiSortMax + 4) * 4 <= 227 * 1024, "shared memory, D = 64");
+
+template <int D>
+__global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                                                           const __grid_constant__ CUtensorMap tmap_v,
+                                                                           const MultiParams p) {
+    using Lay = ChunkLayout<D>;
+    constexpr int NT = kChThreads, TOK = kChTok, NK = Lay::KST, NV = Lay::VST, HALVES = Lay::HALVES;
+    constexpr int BOXES = TOK / kTileTokens;  // 16-token boxes per tile
+    // mbarriers: K and V rings full / empty; per score buffer written / read; P written /
+    // read (its product complete); Q stored; every MMA complete
+    enum { KFULL = 0, KEMPTY = NK, VFULL = 2 * NK, VEMPTY = 2 * NK + NV, SFULL = 2 * NK + 2 * NV, SFREE = SFULL + 2,
+           PFULL = SFREE + 2, PFREE = PFULL + 1, QREADY = PFREE + 1, DONE = QREADY + 1 };
+    static_assert(DONE + 1 == Lay::NBARS, "barrier count");
+
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // swizzled operands need 1 KiB alignment
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + uint32_t(Lay::BARS + 8 * i); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
+    volatile int* bad = reinterpret_cast<volatile int*>(smem + Lay::MISC + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::MISC + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Hkv = p.num_kv_heads, G = p.group, Q = p.q_len, RR = p.rows, Hq = p.num_q_heads;
+    const int nrt = (RR + kChRows - 1) / kChRows;  // row tiles per (sequence, kv head)
+    const int rt = blockIdx.x % nrt;
+    const int item = blockIdx.x / nrt;
+    const int kvh = item % Hkv;
+    const int seq = p.sorted ? multi_sorted_seq<NT>(p, item / Hkv) : item / Hkv;
+    const int L = __ldg(p.context_lens + seq);
+    const int r0 = rt * kChRows;                     // the CTA's first query row
+    const int nrows = min(kChRows, RR - r0);          // its rows
+    auto out_row = [&](int r) -> float* {             // query row r = j * G + h
+        const int j = r / G, h = r - (r / G) * G;
+        return p.out + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D;
+    };
+    if (L < 0 || (long long)L > (long long)p.max_blocks_per_seq * p.block_size) {
+        if (threadIdx.x == 0) set_error(p.err, ERR_BOUNDS);
+        for (int e = threadIdx.x; e < nrows * D; e += NT) out_row(r0 + e / D)[e % D] = NAN;
+        return;
+    }
+    const int lim0 = L - Q + 1;  // row r sees the tokens t < lim0 + r / G (none when that is <= 0)
+    const int tmax = max(0, lim0 + (r0 + nrows - 1) / G);  // tokens some row of the CTA sees
+    const int nt = (tmax + TOK - 1) / TOK;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Lay::NBARS; ++i) {
+            int count = 1;                                                                    // commits
+            if (i == SFREE || i == SFREE + 1 || i == PFULL || i == QREADY) count = kChMath;  // the softmax warps
+            mbar_init(bar(i), count);
+        }
+        *bad = 0;
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == kChMmaWarp) tmem_alloc(smem_u32(tmem_slot), kChCols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        set_error(p.err, ERR_TIMEOUT);
+    };
+    // Bounded wait; false once this or another role has given up.
+    auto wait = [&](int i, uint32_t parity) -> bool {
+        const uint32_t b = bar(i);
+        if (mbar_try_wait(b, parity)) return true;
+        if (*abort_flag) return false;
+        const uint64_t start = global_timer_ns();
+        for (uint32_t it = 1;; ++it) {
+            if (mbar_try_wait(b, parity)) return true;
+            if ((it & 63u) == 0u) {
+                if (*abort_flag) return false;
+                if (global_timer_ns() - start > p.wait_limit_ns) {
+                    give_up();
+                    return false;
+                }
+            }
+        }
+    };
+
+    if (warp > kChMmaWarp) {
+        // ---- producer warps: warp 5 copies K, warp 6 V.  The warp loads the table entries of
+        // 32 boxes (4 tiles) a batch ahead: lane l holds box 32 b + l.
+        const bool is_v = warp - kChMmaWarp - 1 == 1;
+        const int NS = is_v ? NV : NK;
+        const int FULLB = is_v ? VFULL : KFULL, EMPTYB = is_v ? VEMPTY : KEMPTY;
+        const uint32_t ring = sbase + uint32_t(is_v ? Lay::VRING : Lay::KRING);
+        const CUtensorMap* map = is_v ? &tmap_v : &tmap_k;
+        const int32_t* trow = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
+        const int bs = p.block_size, bshift = p.block_shift;
+        auto block_index = [&](int tok) { return bshift >= 0 ? (tok >> bshift) : (tok / bs); };
+        auto block_offset = [&](int tok) { return bshift >= 0 ? (tok & (bs - 1)) : (tok % bs); };
+        auto batch = [&](int b) {  // entry of box 32 b + lane (0 past the tokens the CTA reads)
+            const int tok = (32 * b + lane) * kTileTokens;
+            return tok < tmax ? __ldg(trow + block_index(tok)) : 0;
+        };
+        constexpr int TPB = 32 / BOXES;  // tiles per batch
+        const uint64_t policy = l2_policy_evict_first();
+        int ent_cur = batch(0), ent_nxt = nt > TPB ? batch(1) : 0;
+        int issued = 0;
+        for (int j = 0; j < nt; ++j) {
+            if (j > 0 && j % TPB == 0) {
+                ent_cur = ent_nxt;
+                ent_nxt = batch(j / TPB + 1);
+            }
+            // lane l < BOXES * HALVES copies dim half l % HALVES of box l / HALVES
+            const int bi = lane / HALVES, hf = lane % HALVES;
+            const int el = __shfl_sync(FULL_MASK, ent_cur, ((j % TPB) * BOXES + bi) & 31);
+            const int tok = j * TOK + bi * kTileTokens;
+            const bool live = lane < BOXES * HALVES && tok < tmax;
+            const bool good = live && el >= 0 && (long long)el < p.num_blocks;
+            if (live && !good) {
+                *bad = 1;
+                set_error(p.err, ERR_BOUNDS);
+            }
+            const int s = j % NS;
+            bool ok = true;
+            if (lane == 0 && j >= NS) ok = wait(EMPTYB + s, ((j / NS) - 1) & 1);
+            if (!__shfl_sync(FULL_MASK, ok ? 1 : 0, 0)) break;
+            const uint32_t bytes = uint32_t(__popc(__ballot_sync(FULL_MASK, good))) * kTileTokens * 128u;
+            if (lane == 0) mbar_arrive_expect_tx(bar(FULLB + s), bytes);
+            __syncwarp();  // the byte count is set before any copy can complete
+            if (good)
+                tma_load_2d(ring + uint32_t(s * Lay::TILE + bi * kTileTokens * 128 + hf * Lay::HALF), map, 64 * hf,
+                            (el * Hkv + kvh) * bs + block_offset(tok), bar(FULLB + s), policy);
+            ++issued;
+        }
+        // the CTA may not end with copies in flight: wait for the last fill of each stage
+        if (lane == 0)
+            for (int s = 0; s < NS && s < issued; ++s) {
+                const int jl = s + NS * ((issued - 1 - s) / NS);
+                mbar_wait_bounded(bar(FULLB + s), (jl / NS) & 1, p.wait_limit_ns);
+            }
+        __syncwarp();
+    } else if (warp == kChMmaWarp) {
+        // ---- MMA issuer: P(jp) V(jp) when ready, else S(js) (at most two ahead: two score buffers)
+        constexpr uint32_t IDESC_S = umma_idesc_bf16(kChRows, TOK, 0, 0);
+        constexpr uint32_t IDESC_O = umma_idesc_bf16(kChRows, D, 0, 1);
+        __syncwarp();
+        if (nt > 0) {
+            const bool qok = __all_sync(FULL_MASK, wait(QREADY, 0));
+            (void)qok;
+        }
+        tc_fence_after_sync();
+        int js = 0, jp = 0;
+        uint64_t idle_since = 0;
+        bool idle = false;
+        while (jp < nt) {
+            int act = 0;  // 1: P.V(jp), 2: S(js), -1: give up
+            if (lane == 0) {
+                if (jp < js && mbar_test_wait(bar(PFULL), jp & 1) &&
+                    mbar_test_wait(bar(VFULL + jp % NV), (jp / NV) & 1))
+                    act = 1;
+                // S(js): K landed, and the softmax of tile js - 2 has read the score buffer
+                else if (js < nt && mbar_test_wait(bar(KFULL + js % NK), (js / NK) & 1) &&
+                         (js < 2 || mbar_test_wait(bar(SFREE + (js & 1)), ((js >> 1) - 1) & 1)))
+                    act = 2;
+                else if (*abort_flag) act = -1;
+                else if (!idle) {
+                    idle = true;
+                    idle_since = global_timer_ns();
+                } else if (global_timer_ns() - idle_since > p.wait_limit_ns) {
+                    give_up();
+                    act = -1;
+                }
+                if (act != 0) idle = false;
+            }
+            act = __shfl_sync(FULL_MASK, act, 0);
+            if (act < 0) break;
+            if (act == 0) continue;
+            tc_fence_after_sync();
+            if (act == 2) {
+                if (lane == 0) {
+                    const uint32_t ka = sbase + uint32_t(Lay::KRING + (js % NK) * Lay::TILE);
+                    const uint32_t qa = sbase + uint32_t(Lay::QS);
+                    const uint32_t ts = tmem + ((js & 1) ? kChTS1 : kChTS0);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {  // 16 dims: 32 bytes into the swizzled rows of Q and K
+                        const uint32_t off = uint32_t((kk >> 2) * Lay::HALF + (kk & 3) * 32);
+                        umma_bf16(ts, umma_desc_sw128(qa + off, 16, 1024), umma_desc_sw128(ka + off, 16, 1024),
+                                  IDESC_S, kk > 0);
+                    }
+                    umma_commit(bar(SFULL + (js & 1)));
+                    umma_commit(bar(KEMPTY + js % NK));
+                }
+                ++js;
+            } else {
+                const uint32_t voff = uint32_t(Lay::VRING + (jp % NV) * Lay::TILE);
+                // rows past the sequence hold other data (or poison), and boxes past the CTA's last
+                // token were not copied: zero V there so that 0 * V stays 0
+                const int vend = min(L, (tmax + kTileTokens - 1) / kTileTokens * kTileTokens);
+                const int nvalid = min(TOK, vend - jp * TOK);
+                if (nvalid < TOK) {
+                    for (int e = lane; e < (TOK - nvalid) * 8 * HALVES; e += 32) {
+                        const int r = nvalid + e / (8 * HALVES), c = e % (8 * HALVES);
+                        *reinterpret_cast<uint4*>(smem + voff + (c >> 3) * Lay::HALF + r * 128 + (c & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    tc_fence_after_sync();
+                }
+                if (lane == 0) {
+                    const uint32_t va = sbase + voff;
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)      // P hi, then P lo, against the same V
+#pragma unroll
+                        for (int kk = 0; kk < TOK / 16; ++kk)  // 16 tokens: 8 TMEM columns of P, 2 KiB of V
+                            umma_bf16_tmem_a(tmem + kChTO, tmem + kChTP + uint32_t(64 * part + 8 * kk),
+                                             umma_desc_sw128(va + kk * 2048, Lay::HALF, 1024), IDESC_O,
+                                             (jp | part | kk) != 0);
+                    umma_commit(bar(PFREE));
+                    umma_commit(bar(VEMPTY + jp % NV));
+                }
+                ++jp;
+            }
+            __syncwarp();
+        }
+        // every MMA of the CTA is complete before O is read and tensor memory released
+        if (lane == 0) {
+            umma_commit(bar(DONE));
+            mbar_wait_bounded(bar(DONE), 0, p.wait_limit_ns);
+        }
+        __syncwarp();
+    } else {
+        // ---- softmax warpgroup: thread rl = 32 warp + lane holds query row r0 + rl
+        const int rl = threadIdx.x;
+        const int r = r0 + rl;
+        const bool is_row = rl < nrows;
+        const uint32_t tl = tmem + (uint32_t(warp * 32) << 16);  // this warp's TMEM lane quarter
+
+        // this row of Q into its swizzled K-major tile (zero past the CTA's rows); all loads in
+        // flight before the stores
+        {
+            constexpr int CH = D / 8;  // 16-byte chunks per row
+            uint4 v[CH];
+            const uint4* src = nullptr;
+            if (is_row) {
+                const int j = r / G, h = r - (r / G) * G;
+                src = reinterpret_cast<const uint4*>(p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D);
+            }
+#pragma unroll
+            for (int c = 0; c < CH; ++c) v[c] = is_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+                *reinterpret_cast<uint4*>(smem + Lay::QS + (c >> 3) * Lay::HALF + rl * 128 +
+                                          (((c & 7) ^ (rl & 7)) << 4)) = v[c];
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(QREADY));
+
+        const int lim = is_row ? lim0 + r / G : 0;  // tokens t < lim are visible to this row
+        float m_ref = -INFINITY;                   // reference maximum (log2 units)
+        float l_sum = 0.f;                         // sum of the probabilities, relative to m_ref
+        for (int j = 0; j < nt; ++j) {
+            const int b = j & 1;
+            wait(SFULL + b, (j >> 1) & 1);
+            __syncwarp();
+            tc_fence_after_sync();
+            float y[kChTok];
+#pragma unroll
+            for (int q = 0; q < kChTok / 32; ++q) {
+                uint32_t v[32];
+                tmem_ld_x32(tl + (b ? kChTS1 : kChTS0) + uint32_t(32 * q), v);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) y[32 * q + c] = __uint_as_float(v[c]) * p.scale_log2;
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(SFREE + b));
+
+            const int t0 = j * TOK;
+            if (t0 + TOK > lim) {  // tokens this row may not see (or past the sequence)
+#pragma unroll
+                for (int c = 0; c < kChTok; ++c)
+                    if (t0 + c >= lim) y[c] = -INFINITY;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kChTok; ++c) mx = fmaxf(mx, y[c]);
+            // move the reference only when a score exceeds it by more than the margin (any visible
+            // score when there is none yet); the probabilities stay below 2^8
+            float alpha = 1.f;
+            bool rescale = false;
+            if (mx > m_ref + kChRescale) {
+                alpha = exp2_approx(m_ref - mx);  // no reference yet: 0
+                rescale = j > 0;
+                l_sum *= alpha;
+                m_ref = mx;
+            }
+            const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+            uint32_t ph[kChTok / 2], pl[kChTok / 2];
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < kChTok / 2; ++e) {
+                const float a = exp2_approx(y[2 * e] - ref), c = exp2_approx(y[2 * e + 1] - ref);
+                s0 += a;
+                s1 += c;
+                ph[e] = pack_bf16x2(a, c);
+                pl[e] = pack_bf16x2(a - __uint_as_float(ph[e] << 16), c - __uint_as_float(ph[e] & 0xffff0000u));
+            }
+            l_sum += s0 + s1;
+            // the previous P.V -- the last reader of P and writer of O -- is complete
+            if (j > 0) wait(PFREE, (j - 1) & 1);
+            __syncwarp();
+            tc_fence_after_sync();
+            if (__any_sync(FULL_MASK, rescale)) {
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t v[32];
+                    tmem_ld_x32(tl + kChTO + uint32_t(32 * q), v);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
+                    tmem_st_x32(tl + kChTO + uint32_t(32 * q), v);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint32_t w[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) w[c] = ph[32 * q + c];
+                tmem_st_x32(tl + kChTP + uint32_t(32 * q), w);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) w[c] = pl[32 * q + c];
+                tmem_st_x32(tl + kChTP + uint32_t(64 + 32 * q), w);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(PFULL));
+        }
+
+        // ---- epilogue: O / l once every MMA is complete
+        if (nt > 0) wait(DONE, 0);
+        __syncwarp();
+        tc_fence_after_sync();
+        const bool failed = *bad != 0 || *abort_flag != 0;
+        const float inv = l_sum == 0.f ? 0.f : 1.f / l_sum;  // no token: 0; a NaN input stays NaN
+        float* dst = is_row ? out_row(r) : nullptr;
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+            uint32_t v[32];
+            if (nt > 0) {
+                tmem_ld_x32(tl + kChTO + uint32_t(32 * q), v);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) v[c] = 0u;
+            }
+            if (is_row) {
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                    float4 o = make_float4(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv,
+                                           __uint_as_float(v[c + 2]) * inv, __uint_as_float(v[c + 3]) * inv);
+                    if (nt == 0) o = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (failed) o = make_float4(NAN, NAN, NAN, NAN);
+                    *reinterpret_cast<float4*>(dst + 32 * q + c) = o;
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == kChMmaWarp) tmem_dealloc(tmem, kChCols);
+}
+
+template <int D>
+static cudaError_t launch_chunk_d(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p,
+                                  cudaStream_t stream) {
+    using Lay = ChunkLayout<D>;
+    auto kern = paged_chunk_query_kernel<D>;
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit == 0 || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Lay::ALLOC));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const long long nrt = (p.rows + kChRows - 1) / kChRows;
+    const long long grid = (long long)p.num_seqs * p.num_kv_heads * nrt;
+    if (grid > INT32_MAX) return cudaErrorInvalidValue;
+    kern<<<unsigned(grid), kChThreads, Lay::ALLOC, stream>>>(mk, mv, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p, int head_dim,
+                         cudaStream_t stream) {
+    if (head_dim == 128) return launch_chunk_d<128>(mk, mv, p, stream);
+    if (head_dim == 64) return launch_chunk_d<64>(mk, mv, p, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pf

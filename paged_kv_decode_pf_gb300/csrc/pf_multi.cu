@@ -36,56 +36,11 @@
 #include "pf_device.cuh"
 #include "pf_tcgen05.cuh"
 #include "pf_internal.h"
+#include "pf_multi.cuh"
 
 namespace pf {
 
 constexpr int kMultiMaxRows = 16;  // g * q_len: one m16 tile of query rows
-
-struct MultiParams {
-    const uint16_t* q;          // [S, q_len, Hq, D]
-    const int32_t* block_tables;
-    const int32_t* context_lens;
-    float* out;                 // [S, q_len, Hq, D]
-    unsigned* err;
-    long long num_blocks;
-    unsigned long long wait_limit_ns;
-    float scale_log2;
-    int num_seqs, q_len, num_q_heads, num_kv_heads, group, rows;
-    int block_size, block_shift, max_blocks_per_seq;
-    int sorted;  // CTA b serves the sequence of rank b / Hkv, longest first (num_seqs <= kMultiSortMax)
-};
-
-constexpr int kMultiSortMax = 512;
-
-// The sequence of rank r when the sequences are ordered longest first (ties by index):
-// every CTA ranks the lengths in shared memory, so the hardware's in-order dispatch of
-// the grid starts the longest items first and they do not form the launch's tail.
-template <int NT>
-__device__ __forceinline__ int multi_sorted_seq(const MultiParams& p, int r) {
-    __shared__ __align__(16) int keys[kMultiSortMax];
-    __shared__ int s_seq;
-    const int S = p.num_seqs, Sp = (S + 3) & ~3;
-    for (int i = threadIdx.x; i < Sp; i += NT) {
-        int key = -1;
-        if (i < S) {
-            const int Li = min(max(__ldg(p.context_lens + i), 0), (1 << 20) - 1);
-            key = (Li << 10) | (1023 - i);
-        }
-        keys[i] = key;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < S; i += NT) {
-        const int ki = keys[i];
-        int rank = 0;
-        for (int j = 0; j < Sp; j += 4) {
-            const int4 kj = *reinterpret_cast<const int4*>(keys + j);
-            rank += int(kj.x > ki) + int(kj.y > ki) + int(kj.z > ki) + int(kj.w > ki);
-        }
-        if (rank == r) s_seq = i;
-    }
-    __syncthreads();
-    return s_seq;
-}
 
 template <int D, int NW, int NST>
 struct MultiLayout {
@@ -1530,7 +1485,7 @@ static pf_status multi_query_setup(const void* q, const void* k_cache, const voi
     const int group = num_q_heads / num_kv_heads;
     if (head_dim != 64 && head_dim != 128) return PF_ERR_UNSUPPORTED;
     if (block_size % kTileTokens != 0) return PF_ERR_UNSUPPORTED;
-    if ((long long)group * q_len > kWideMaxRows) return PF_ERR_UNSUPPORTED;
+    if ((long long)group * q_len > kChunkMaxRows) return PF_ERR_UNSUPPORTED;
     const long long rows = num_blocks * num_kv_heads * (long long)block_size;
     if (rows > INT32_MAX || (long long)num_seqs * num_kv_heads > INT32_MAX) return PF_ERR_UNSUPPORTED;
     auto al = [](const void* ptr, size_t a) { return ptr != nullptr && reinterpret_cast<uintptr_t>(ptr) % a == 0; };
@@ -1579,7 +1534,9 @@ extern "C" pf_status pf_paged_attention_multi_query(const void* q, const void* k
     if (st != PF_OK || num_seqs == 0) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (head_dim == 64)
+    if (p.rows >= kChunkMinRows)
+        e = launch_chunk(mk, mv, p, head_dim, s);  // prompt chunks: query rows on the tcgen05 M side
+    else if (head_dim == 64)
         e = launch_multi_any<64>(mk, mv, p, s);
     else if (p.rows <= 32)
         e = launch_multi_any<128>(mk, mv, p, s);
@@ -1602,6 +1559,7 @@ extern "C" pf_status pf_paged_attention_multi_query_tcgen05(const void* q, const
     if (st != PF_OK) return st;
     if (head_dim != 128) return PF_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PF_OK;
-    const cudaError_t e = launch_multi_tc(mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = p.rows >= kChunkMinRows ? launch_chunk(mk, mv, p, head_dim, s) : launch_multi_tc(mk, mv, p, s);
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }

@@ -127,9 +127,10 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
 
 
 def test_multi_query_host_validation(lib):
-    """Both multi-token entry points check their shapes on the host: more than 64 query rows per kv
-    head, a head_dim outside {64, 128} or a block size not a multiple of 16 launch nothing; the
-    tcgen05 form takes head_dim 128 only; no sequence is a no-op."""
+    """Both multi-token entry points check their shapes on the host: more than 65 536 query rows per
+    kv head, a head_dim outside {64, 128} or a block size not a multiple of 16 launch nothing; the
+    tcgen05 form takes head_dim 128 only; no sequence is a no-op (also past 64 rows per kv head,
+    where the prompt-chunk kernel would run)."""
     P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
     for name in ("pf_paged_attention_multi_query", "pf_paged_attention_multi_query_tcgen05"):
         f = getattr(lib, name)
@@ -138,7 +139,9 @@ def test_multi_query_host_validation(lib):
         # q, k, v, tables, lengths, S, q_len, Hq, Hkv, D, bs, max_blocks, num_blocks, scale, out, stream
         args = [None] * 5 + [0, 4, 32, 8, 128, 16, 8, 64, 0.088, None, None]
         assert f(*args) == 0                                          # no sequence: nothing to do
-        assert f(*(args[:6] + [17] + args[7:])) == 2                  # 4 x 17 = 68 rows per kv head
+        assert f(*(args[:6] + [17] + args[7:])) == 0                  # 4 x 17 = 68 rows: prompt chunk, no sequence
+        assert f(*(args[:6] + [16384] + args[7:])) == 0               # 65 536 rows: the limit
+        assert f(*(args[:6] + [16385] + args[7:])) == 2               # 65 540 rows per kv head
         assert f(*(args[:9] + [96] + args[10:])) == 2                 # head_dim 96
         assert f(*(args[:10] + [24] + args[11:])) == 2                # block size not a multiple of 16
         assert f(*(args[:6] + [0] + args[7:])) == 1                   # q_len 0

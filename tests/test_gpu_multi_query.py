@@ -90,15 +90,6 @@ def test_multi_query_wide_bad_block_and_length(pf, oracle_lib, kernel):
     check_close(got[[0, 3]], ref[[0, 3]])
 
 
-def test_multi_query_rows_beyond_sixty_four_are_unsupported(pf):
-    wl = make_workload("mqx", 2, 32, 8, 128, 16, [40, 50], seed=103)
-    d = to_device(wl)
-    q = torch.zeros((2, 17, 32, 128), dtype=torch.bfloat16, device="cuda")     # g=4 x 17 = 68 rows
-    with pytest.raises(pf.PFError) as e:
-        pf.paged_attention_multi_query(q, d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"])
-    assert e.value.status == pf.PF_ERR_UNSUPPORTED
-
-
 @pytest.mark.parametrize("q_len,kernel", [(4, "auto"), (8, "auto"), (16, "auto")])
 def test_multi_query_llama3_full_size(pf, oracle_lib, config_workload, q_len, kernel):
     """The launches the bench times: all 256 Llama-3-shaped sequences (4.8 GB of K/V) with 4, 8
