@@ -10,10 +10,10 @@
 // cores rather than by HBM.  Here the query rows are the M side of single-CTA tcgen05.mma:
 //     S(j)  = Q K(j)^T        M = 128 rows, N = 128 tokens, K = D
 //     O    += P(j) V(j)       M = 128 rows, N = D,          K = 128 tokens
-// with Q and the K / V tiles in shared memory (TMA tiles with the 128-byte swizzle) and S,
-// P and O in tensor memory.  P enters the product as its bf16 high part and the bf16
-// remainder (two MMAs against the same V tile), so the probabilities keep about 16
-// significant bits, as in the other multi-token kernels.
+// with the K / V tiles in shared memory (TMA tiles with the 128-byte swizzle) and Q, S, P
+// and O in tensor memory (Q and P as the A operands).  P enters the product as its bf16
+// high part and the bf16 remainder (two MMAs against the same V tile), so the
+// probabilities keep about 16 significant bits, as in the other multi-token kernels.
 //
 // One CTA per (sequence, kv head, tile of 128 rows); the row tiles of one (sequence, kv
 // head) are consecutive in the grid so that they stream the same K/V tiles at about the
@@ -21,14 +21,17 @@
 //  * warps 0-3 (the softmax warpgroup): thread 32 w + l holds query row 32 w + l of the
 //    tile, which is lane 32 w + l of tensor memory, so a row's maximum and sum never leave
 //    its thread.  Per tile it reads its 128 scores, masks the tokens its row may not see,
-//    and moves its reference maximum only when a score exceeds it by more than 2^8 (the
-//    rescale of its O row then happens once the previous P.V is complete); it writes its
-//    probabilities' hi and lo parts into tensor memory as the A operand of P.V;
+//    and moves its reference maximum only when a score exceeds it by more than 2^8; it
+//    writes the probabilities' hi and lo parts over the scores it read, as the A operand of
+//    P.V.  Only a move of the reference makes it wait for the previous P.V (to rescale its
+//    O row); otherwise P(j) V(j) queues behind P(j - 1) V(j - 1) on the tensor pipe;
 //  * warp 4 issues the MMAs from one lane: S(j + 1) into the second score buffer while the
-//    softmax works on S(j), and P(j) V(j) as soon as P(j) is written;
+//    softmax works on S(j), and P(j) V(j) as soon as P(j) is written; S(j + 2) reuses the
+//    buffer of S(j) once P(j) V(j) is complete;
 //  * warp 5 copies K tiles into a ring of KST stages and warp 6 V tiles into one of VST: a
 //    tile is eight 16-token boxes, and each box and dim half is one TMA copy issued by its
 //    own lane (copies of one thread to scattered pages are served one after another).
+//    With Q in tensor memory the shared memory holds three stages of each.
 // Every wait is bounded; one that gives up raises an abort flag that ends the others, and
 // every role still runs to its end, so tensor memory is always released.
 #include <atomic>
@@ -53,18 +56,18 @@ constexpr int kChMmaWarp = kChMath;
 constexpr int kChProducers = 2;    // one warp copies K, one copies V
 constexpr int kChThreads = 32 * (kChMath + 1 + kChProducers);
 constexpr float kChRescale = 8.f;  // the reference maximum moves when a score exceeds it by more (log2 units)
-// tensor memory columns: score buffers, P (hi, lo), O
-constexpr uint32_t kChTS0 = 0, kChTS1 = 128, kChTP = 256, kChTO = 384, kChCols = 512;
+// tensor memory columns: two score buffers (each later holds its tile's P: hi in the first 64
+// columns, lo in the next 64), O (D columns), Q (D / 2 columns: two bf16 per column)
+constexpr uint32_t kChTS0 = 0, kChTS1 = 128, kChTO = 256, kChTQ = 384, kChCols = 512;
 
 template <int D>
 struct ChunkLayout {
     static constexpr int HALVES = D / 64;              // 128-byte swizzle rows per token (or query) row
     static constexpr int HALF = kChTok * 128;          // 128 rows of 128 bytes: 16 KiB
-    static constexpr int TILE = HALVES * HALF;         // the Q tile, or one K or V tile
-    static constexpr int KST = D == 128 ? 3 : 5;       // K ring depth
-    static constexpr int VST = D == 128 ? 2 : 4;       // V ring depth
-    static constexpr int QS = 0;
-    static constexpr int KRING = QS + TILE;
+    static constexpr int TILE = HALVES * HALF;         // one K or V tile
+    static constexpr int KST = D == 128 ? 3 : 6;       // K ring depth
+    static constexpr int VST = D == 128 ? 3 : 6;       // V ring depth
+    static constexpr int KRING = 0;
     static constexpr int VRING = KRING + KST * TILE;
     static constexpr int NBARS = 2 * KST + 2 * VST + 8;
     static constexpr int BARS = VRING + VST * TILE;
@@ -82,10 +85,10 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
     using Lay = ChunkLayout<D>;
     constexpr int NT = kChThreads, TOK = kChTok, NK = Lay::KST, NV = Lay::VST, HALVES = Lay::HALVES;
     constexpr int BOXES = TOK / kTileTokens;  // 16-token boxes per tile
-    // mbarriers: K and V rings full / empty; per score buffer written / read; P written /
-    // read (its product complete); Q stored; every MMA complete
-    enum { KFULL = 0, KEMPTY = NK, VFULL = 2 * NK, VEMPTY = 2 * NK + NV, SFULL = 2 * NK + 2 * NV, SFREE = SFULL + 2,
-           PFULL = SFREE + 2, PFREE = PFULL + 1, QREADY = PFREE + 1, DONE = QREADY + 1 };
+    // mbarriers: K and V rings full / empty; per score buffer: S written, P written, P.V
+    // complete (the buffer free again); Q stored; every MMA complete
+    enum { KFULL = 0, KEMPTY = NK, VFULL = 2 * NK, VEMPTY = 2 * NK + NV, SFULL = 2 * NK + 2 * NV, PFULL = SFULL + 2,
+           PFREE = PFULL + 2, QREADY = PFREE + 2, DONE = QREADY + 1 };
     static_assert(DONE + 1 == Lay::NBARS, "barrier count");
 
     extern __shared__ unsigned char smem_raw[];
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
     if (threadIdx.x == 0) {
         for (int i = 0; i < Lay::NBARS; ++i) {
             int count = 1;                                                                    // commits
-            if (i == SFREE || i == SFREE + 1 || i == PFULL || i == QREADY) count = kChMath;  // the softmax warps
+            if (i == PFULL || i == PFULL + 1 || i == QREADY) count = kChMath;  // the softmax warps
             mbar_init(bar(i), count);
         }
         *bad = 0;
@@ -228,12 +231,12 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
         while (jp < nt) {
             int act = 0;  // 1: P.V(jp), 2: S(js), -1: give up
             if (lane == 0) {
-                if (jp < js && mbar_test_wait(bar(PFULL), jp & 1) &&
+                if (jp < js && mbar_test_wait(bar(PFULL + (jp & 1)), (jp >> 1) & 1) &&
                     mbar_test_wait(bar(VFULL + jp % NV), (jp / NV) & 1))
                     act = 1;
-                // S(js): K landed, and the softmax of tile js - 2 has read the score buffer
+                // S(js): K landed, and P(js - 2) V(js - 2) -- the last reader of the buffer -- is complete
                 else if (js < nt && mbar_test_wait(bar(KFULL + js % NK), (js / NK) & 1) &&
-                         (js < 2 || mbar_test_wait(bar(SFREE + (js & 1)), ((js >> 1) - 1) & 1)))
+                         (js < 2 || mbar_test_wait(bar(PFREE + (js & 1)), ((js >> 1) - 1) & 1)))
                     act = 2;
                 else if (*abort_flag) act = -1;
                 else if (!idle) {
@@ -252,14 +255,12 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
             if (act == 2) {
                 if (lane == 0) {
                     const uint32_t ka = sbase + uint32_t(Lay::KRING + (js % NK) * Lay::TILE);
-                    const uint32_t qa = sbase + uint32_t(Lay::QS);
                     const uint32_t ts = tmem + ((js & 1) ? kChTS1 : kChTS0);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {  // 16 dims: 32 bytes into the swizzled rows of Q and K
-                        const uint32_t off = uint32_t((kk >> 2) * Lay::HALF + (kk & 3) * 32);
-                        umma_bf16(ts, umma_desc_sw128(qa + off, 16, 1024), umma_desc_sw128(ka + off, 16, 1024),
-                                  IDESC_S, kk > 0);
-                    }
+                    for (int kk = 0; kk < D / 16; ++kk)  // 16 dims: 8 TMEM columns of Q, 32 bytes into K's rows
+                        umma_bf16_tmem_a(ts, tmem + kChTQ + uint32_t(8 * kk),
+                                         umma_desc_sw128(ka + uint32_t((kk >> 2) * Lay::HALF + (kk & 3) * 32), 16, 1024),
+                                         IDESC_S, kk > 0);
                     umma_commit(bar(SFULL + (js & 1)));
                     umma_commit(bar(KEMPTY + js % NK));
                 }
@@ -282,14 +283,15 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
                 }
                 if (lane == 0) {
                     const uint32_t va = sbase + voff;
+                    const uint32_t tp = tmem + ((jp & 1) ? kChTS1 : kChTS0);
 #pragma unroll
                     for (int part = 0; part < 2; ++part)      // P hi, then P lo, against the same V
 #pragma unroll
                         for (int kk = 0; kk < TOK / 16; ++kk)  // 16 tokens: 8 TMEM columns of P, 2 KiB of V
-                            umma_bf16_tmem_a(tmem + kChTO, tmem + kChTP + uint32_t(64 * part + 8 * kk),
+                            umma_bf16_tmem_a(tmem + kChTO, tp + uint32_t(64 * part + 8 * kk),
                                              umma_desc_sw128(va + kk * 2048, Lay::HALF, 1024), IDESC_O,
                                              (jp | part | kk) != 0);
-                    umma_commit(bar(PFREE));
+                    umma_commit(bar(PFREE + (jp & 1)));
                     umma_commit(bar(VEMPTY + jp % NV));
                 }
                 ++jp;
@@ -309,56 +311,78 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
         const bool is_row = rl < nrows;
         const uint32_t tl = tmem + (uint32_t(warp * 32) << 16);  // this warp's TMEM lane quarter
 
-        // this row of Q into its swizzled K-major tile (zero past the CTA's rows); all loads in
-        // flight before the stores
+        // this row of Q into tensor memory (two bf16 per column; zero past the CTA's rows)
         {
             constexpr int CH = D / 8;  // 16-byte chunks per row
-            uint4 v[CH];
-            const uint4* src = nullptr;
+            uint32_t w[D / 2];
             if (is_row) {
                 const int j = r / G, h = r - (r / G) * G;
-                src = reinterpret_cast<const uint4*>(p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D);
+                const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t(seq) * Q + j) * Hq + kvh * G + h) * D);
+#pragma unroll
+                for (int c = 0; c < CH; ++c) {
+                    const uint4 v = __ldg(src + c);
+                    w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < D / 2; ++c) w[c] = 0u;
             }
 #pragma unroll
-            for (int c = 0; c < CH; ++c) v[c] = is_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            for (int q = 0; q < D / 64; ++q) {
+                uint32_t x[32];
 #pragma unroll
-            for (int c = 0; c < CH; ++c)
-                *reinterpret_cast<uint4*>(smem + Lay::QS + (c >> 3) * Lay::HALF + rl * 128 +
-                                          (((c & 7) ^ (rl & 7)) << 4)) = v[c];
+                for (int c = 0; c < 32; ++c) x[c] = w[32 * q + c];
+                tmem_st_x32(tl + kChTQ + uint32_t(32 * q), x);
+            }
+            tmem_st_wait();
         }
-        fence_proxy_async_smem();
+        tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(QREADY));
 
         const int lim = is_row ? lim0 + r / G : 0;  // tokens t < lim are visible to this row
         float m_ref = -INFINITY;                   // reference maximum (log2 units)
         float l_sum = 0.f;                         // sum of the probabilities, relative to m_ref
+        const float sc = p.scale_log2;
+        // a positive scale commutes with the maximum: the row maximum of the raw scores, and
+        // one FFMA per score inside the exponent; otherwise (zero or negative scale) the
+        // scores are scaled first
+        const bool pos = sc > 0.f;
         for (int j = 0; j < nt; ++j) {
             const int b = j & 1;
+            const uint32_t tsb = tl + (b ? kChTS1 : kChTS0);
             wait(SFULL + b, (j >> 1) & 1);
             __syncwarp();
             tc_fence_after_sync();
             float y[kChTok];
+            {
+                uint32_t v[kChTok];
+                tmem_ld_x128(tsb, v);
 #pragma unroll
-            for (int q = 0; q < kChTok / 32; ++q) {
-                uint32_t v[32];
-                tmem_ld_x32(tl + (b ? kChTS1 : kChTS0) + uint32_t(32 * q), v);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) y[32 * q + c] = __uint_as_float(v[c]) * p.scale_log2;
+                for (int c = 0; c < kChTok; ++c) y[c] = __uint_as_float(v[c]);
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(SFREE + b));
-
+            if (!pos) {
+#pragma unroll
+                for (int c = 0; c < kChTok; ++c) y[c] *= sc;
+            }
             const int t0 = j * TOK;
             if (t0 + TOK > lim) {  // tokens this row may not see (or past the sequence)
 #pragma unroll
                 for (int c = 0; c < kChTok; ++c)
                     if (t0 + c >= lim) y[c] = -INFINITY;
             }
-            float mx = -INFINITY;
+            // row maximum in log2 units, as a tree (8 independent chains)
+            float mx;
+            {
+                float m8[8];
 #pragma unroll
-            for (int c = 0; c < kChTok; ++c) mx = fmaxf(mx, y[c]);
+                for (int i = 0; i < 8; ++i) m8[i] = y[i];
+#pragma unroll
+                for (int c = 8; c < kChTok; ++c) m8[c & 7] = fmaxf(m8[c & 7], y[c]);
+                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                if (pos) mx *= sc;  // -inf stays -inf
+            }
             // move the reference only when a score exceeds it by more than the margin (any visible
             // score when there is none yet); the probabilities stay below 2^8
             float alpha = 1.f;
@@ -370,22 +394,29 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
                 m_ref = mx;
             }
             const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+            const float ysc = pos ? sc : 1.f;  // exponent: y * ysc - ref
+            // probabilities as a bf16 high part (truncation: the top 16 bits) and the bf16 rounding
+            // of the exact remainder, so that hi + lo carries about 16 significant bits
             uint32_t ph[kChTok / 2], pl[kChTok / 2];
-            float s0 = 0.f, s1 = 0.f;
+            float s8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s8[i] = 0.f;
 #pragma unroll
             for (int e = 0; e < kChTok / 2; ++e) {
-                const float a = exp2_approx(y[2 * e] - ref), c = exp2_approx(y[2 * e + 1] - ref);
-                s0 += a;
-                s1 += c;
-                ph[e] = pack_bf16x2(a, c);
-                pl[e] = pack_bf16x2(a - __uint_as_float(ph[e] << 16), c - __uint_as_float(ph[e] & 0xffff0000u));
+                const float a = exp2_approx(fmaf(y[2 * e], ysc, -ref));
+                const float c = exp2_approx(fmaf(y[2 * e + 1], ysc, -ref));
+                s8[(2 * e) & 7] += a;
+                s8[(2 * e + 1) & 7] += c;
+                const uint32_t ua = __float_as_uint(a), uc = __float_as_uint(c);
+                ph[e] = __byte_perm(ua, uc, 0x7632);  // high halves: element 2e low, 2e + 1 high
+                pl[e] = pack_bf16x2(a - __uint_as_float(ua & 0xffff0000u), c - __uint_as_float(uc & 0xffff0000u));
             }
-            l_sum += s0 + s1;
-            // the previous P.V -- the last reader of P and writer of O -- is complete
-            if (j > 0) wait(PFREE, (j - 1) & 1);
-            __syncwarp();
-            tc_fence_after_sync();
+            l_sum += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
             if (__any_sync(FULL_MASK, rescale)) {
+                // O is complete up to P(j - 1) V(j - 1) before its rows are rescaled
+                wait(PFREE + ((j - 1) & 1), ((j - 1) >> 1) & 1);
+                __syncwarp();
+                tc_fence_after_sync();
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     uint32_t v[32];
@@ -395,20 +426,21 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
                     tmem_st_x32(tl + kChTO + uint32_t(32 * q), v);
                 }
             }
+            // P over the scores of this buffer: hi in columns 0-63, lo in 64-127
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 uint32_t w[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) w[c] = ph[32 * q + c];
-                tmem_st_x32(tl + kChTP + uint32_t(32 * q), w);
+                tmem_st_x32(tsb + uint32_t(32 * q), w);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) w[c] = pl[32 * q + c];
-                tmem_st_x32(tl + kChTP + uint32_t(64 + 32 * q), w);
+                tmem_st_x32(tsb + uint32_t(64 + 32 * q), w);
             }
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(PFULL));
+            if (lane == 0) mbar_arrive(bar(PFULL + b));
         }
 
         // ---- epilogue: O / l once every MMA is complete
