@@ -196,18 +196,21 @@ class Runner:
             self.sm = torch.from_numpy(wl.slot_mapping).to(dev)
         self.auto = variant == "auto"  # pf_paged_attention_decode_auto with the true longest context
         self.split = not self.auto and (variant == "split" or wl.partition_size is not None)
+        self.cluster = False
         if self.auto:
             self.max_ctx = wl.max_context_len
             self.P, need = pf.decode_auto_plan(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
                                                self.max_ctx, dev)
             self.ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+        # the cluster split: a chunk size and no workspace (one launch)
+        self.cluster = self.auto and self.P > 0 and not need
         if self.split:
             self.P = wl.partition_size or 512
             self.max_ctx = wl.max_context_len
             self.ws = pf.alloc_workspace(wl.num_seqs, wl.num_q_heads, wl.head_dim, self.max_ctx, self.P, dev)
         self.fused = self.append and not self.split and variant == "fused"
         self.kernels_per_step = 1 if self.fused else (1 if self.append else 0) + (
-            2 if self.split or (self.auto and self.P) else 1)
+            2 if self.split or (self.auto and self.P and not self.cluster) else 1)
         self.dominant = "partition" if self.split else ("decode_append" if self.fused else "decode")
 
     def step(self, ev=None):
@@ -568,7 +571,7 @@ def main():
             del mr
         del runner
         torch.cuda.empty_cache()
-        for idx, variant in [(1, "decode"), (2, "decode"), (2, "auto"), (3, "decode"), (3, "fused"), (5, "decode"),
+        for idx, variant in [(1, "decode"), (1, "auto"), (2, "decode"), (2, "auto"), (3, "decode"), (3, "fused"), (5, "decode"),
                              (5, "auto")]:
             if idx == args.workload and variant == "decode":
                 continue
@@ -583,7 +586,7 @@ def main():
             extras[CONFIGS[idx].name + ("_fused" if r.fused else "_auto" if r.auto else "")] = {
                 "description": CONFIGS[idx].description,
                 "step": "append and decode fused in one launch" if r.fused else
-                        (f"decode_auto ({'partition + merge, P=' + str(r.P) if r.P else 'single pass'}, "
+                        (f"decode_auto ({('cluster split, chunk ' + str(r.P) + ' tokens per CTA, one launch') if r.cluster else ('partition + merge, P=' + str(r.P)) if r.P else 'single pass'}, "
                          f"max_context_len {r.max_ctx})") if r.auto else
                         ("append + " if r.append else "") + ("partition + merge" if r.split else "decode"),
                 "us_per_step": round(ms_s * 1e3, 2) if fl is None else None,

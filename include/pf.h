@@ -192,12 +192,15 @@ PF_API pf_status pf_paged_attention_decode_append(const void* q, const void* k_n
  * (g * q_len): up to 16, one CTA's four warps split the tokens (mma.sync); 17 to
  * 32, and 33 to 64 at head_dim 64, each 16-row tile has its own warp and one or
  * two producer warps stream K/V to all of them (mma.sync); 33 to 64 at head_dim
- * 128 run the kernel of pf_paged_attention_multi_query_tcgen05.
+ * 128 run the kernel of pf_paged_attention_multi_query_tcgen05.  Past 64 rows --
+ * a prompt chunk of tens to hundreds of tokens -- the prompt-chunk kernel runs:
+ * one CTA per (sequence, kv head, tile of 128 rows), the rows as the M side of
+ * tcgen05.mma, Q, S, P and O in tensor memory, K and V tiles by TMA.
  *
  *   q    [num_seqs, q_len, num_q_heads, head_dim] bf16, 16-byte aligned
  *   out  [num_seqs, q_len, num_q_heads, head_dim] fp32
  * Supported: head_dim in {64, 128}, block_size a multiple of 16,
- * (num_q_heads / num_kv_heads) * q_len <= 64, num_blocks * num_kv_heads *
+ * (num_q_heads / num_kv_heads) * q_len <= 65536, num_blocks * num_kv_heads *
  * block_size < 2^31; other arguments and errors as pf_paged_attention_decode.
  */
 PF_API pf_status pf_paged_attention_multi_query(const void* q, const void* k_cache, const void* v_cache,
@@ -219,7 +222,8 @@ PF_API pf_status pf_paged_attention_multi_query(const void* q, const void* k_cac
  * it is the faster one (Llama-3-8B-shaped batch: 886 and 905 us at 48 and 64
  * rows against 1,148 and 1,211 us); at 32 rows and below the mma.sync kernels
  * are faster (827 against 864 us at 32 rows), since a 128-token tile's products
- * cost the same whatever the row count.
+ * cost the same whatever the row count.  Past 64 rows this entry runs the same
+ * prompt-chunk kernel as pf_paged_attention_multi_query.
  *
  * Supported: head_dim == 128 (else PF_ERR_UNSUPPORTED); the other shapes,
  * arguments and errors as pf_paged_attention_multi_query.
@@ -292,16 +296,26 @@ PF_API pf_status pf_paged_attention_merge(const void* workspace, const int32_t* 
 
 /*
  * Decode attention that chooses its own decomposition from the sizes the host
- * knows (no device memory is read): the single pass when there are enough
- * (sequence, kv head) items to fill the GPU, otherwise the split over context
- * partitions + merge, with a partition size that gives a long sequence enough
- * partitions.  The result is the same attention (within fp32 rounding).
+ * knows (no device memory is read), one of three:
+ *   - the single pass, when there are enough (sequence, kv head) items to fill
+ *     the GPU or the contexts are short;
+ *   - the cluster split, when the items are few (fewer than half the SMs would
+ *     get one) and a cluster of at most 8 CTAs covers max_context_len in chunks
+ *     of at most 1,024 tokens: each item's CTAs take consecutive chunks, and the
+ *     chunks' partials are merged through distributed shared memory within the
+ *     cluster in the same launch -- no workspace, one kernel;
+ *   - otherwise the split over context partitions + merge, with a partition size
+ *     that gives a long sequence enough partitions (workspace needed).
+ * The result is the same attention (within fp32 rounding).
  *
  * pf_paged_attention_decode_auto_plan() returns the partition size the call
- * will use (0 = single pass) and writes the workspace bytes it needs (0 for
- * the single pass) to *workspace_bytes; it needs the current device (SM count).
+ * will use -- 0 for the single pass, the chunk of each CTA for the cluster split
+ * -- and writes the workspace bytes it needs to *workspace_bytes (0 for the
+ * single pass and the cluster split, which a positive return with 0 bytes
+ * identifies); it needs the current device (SM count).
  * pf_paged_attention_decode_auto takes the decode arguments plus
- * max_context_len (>= every context length) and a workspace of at least that
+ * max_context_len (>= every context length: a longer one flags
+ * PF_ERR_DEVICE_BOUNDS and NaN-fills its rows) and a workspace of at least that
  * size (256-byte aligned; may be NULL when the plan needs none).
  */
 PF_API int pf_paged_attention_decode_auto_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,

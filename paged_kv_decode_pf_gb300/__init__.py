@@ -242,7 +242,9 @@ def paged_attention_multi_query(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
 
 def decode_auto_plan(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                      max_context_len: int, device=None) -> Tuple[int, int]:
-    """(partition size the auto decode will use, 0 = single pass; workspace bytes it needs)."""
+    """(partition size the auto decode will use, workspace bytes it needs): (0, 0) for the single
+    pass, (chunk per CTA, 0) for the cluster split (few items: one launch, no workspace),
+    (partition size, bytes) for the split over context partitions + merge."""
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     ws = ctypes.c_size_t()
     with torch.cuda.device(device):
@@ -254,8 +256,9 @@ def decode_auto_plan(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_di
 def paged_attention_decode_auto(q, k_cache, v_cache, block_tables, context_lens, max_context_len: Optional[int] = None,
                                 scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
                                 out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Decode attention with the decomposition chosen by the library (single pass or split + merge).
-    max_context_len defaults to the table's capacity; a workspace is allocated when the plan needs one."""
+    """Decode attention with the decomposition chosen by the library (single pass, cluster split, or
+    split + merge).  max_context_len defaults to the table's capacity; a workspace is allocated when the
+    plan needs one."""
     S, Hq, Hkv, D, bs, NB, MB = _attn_shapes(q, k_cache, v_cache, block_tables, context_lens)
     if max_context_len is None:
         max_context_len = MB * bs

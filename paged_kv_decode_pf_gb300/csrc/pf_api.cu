@@ -332,6 +332,17 @@ static DecodeParams make_params(const AttnArgs& a, unsigned* err) {
     return p;
 }
 
+// CTA order of the single pass: longest first when the items outnumber the CTAs that are resident
+// at once (three per SM) -- the hardware's in-order dispatch then starts the long items first --
+// and natural otherwise, where every item starts at once and the order cannot matter.
+static int decode_order(int num_seqs, int num_kv_heads) {
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess) sms = 0;
+    const long long items = (long long)num_seqs * num_kv_heads;
+    const bool queued = sms <= 0 || items > 3LL * sms;
+    return (queued && num_seqs > 1 && num_seqs <= kMaxSortedSeqsDecode) ? ORDER_SORTED : ORDER_NATURAL;
+}
+
 static cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int mode, cudaStream_t stream) {
     return head_dim == 64 ? launch_decode_d64(p, group, mode, stream) : launch_decode_d128(p, group, mode, stream);
 }
@@ -416,7 +427,7 @@ pf_status pf_paged_attention_decode(const void* q, const void* k_cache, const vo
     if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
     DecodeParams p = make_params(a, err);
     p.out = out;
-    p.order_mode = (num_seqs > 1 && num_seqs <= kMaxSortedSeqsDecode) ? ORDER_SORTED : ORDER_NATURAL;
+    p.order_mode = decode_order(num_seqs, num_kv_heads);
     const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, MODE_DECODE,
                                         reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
@@ -439,7 +450,7 @@ pf_status pf_paged_attention_decode_append(const void* q, const void* k_new, con
     if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
     DecodeParams p = make_params(a, err);
     p.out = out;
-    p.order_mode = (num_seqs > 1 && num_seqs <= kMaxSortedSeqsDecode) ? ORDER_SORTED : ORDER_NATURAL;
+    p.order_mode = decode_order(num_seqs, num_kv_heads);
     p.k_new = static_cast<const uint16_t*>(k_new);
     p.v_new = static_cast<const uint16_t*>(v_new);
     p.slot_mapping = slot_mapping;
@@ -573,6 +584,27 @@ pf_status pf_debug_bounded_wait(int64_t limit_ns, pf_stream_t stream) {
 namespace pf {
 // Decode CTAs resident per SM at the compiled configuration (shared memory bound).
 constexpr int kDecodeCtasPerSm = 3;
+// Cluster split: at most this many CTAs per item (the portable cluster size) and tokens per CTA.
+constexpr int kClusterMax = kClusterMaxSize;
+constexpr int kClusterMaxChunk = 1024;
+
+// The cluster split applies when the single pass would leave more than half the SMs without
+// an item and a cluster of at most kClusterMax CTAs covers the longest context in chunks of at
+// most kClusterMaxChunk tokens.  C: the largest power of two with items * C <= the resident CTA
+// slots, at most one chunk of 16 tokens per CTA; chunk: tokens per CTA, a multiple of 16.
+static bool cluster_plan(long long items, int sms, int max_context_len, int* C_out, int* chunk_out) {
+    if (items <= 0 || items * 2 > sms || max_context_len < 2 * kTileTokens) return false;
+    const long long slots = (long long)sms * kDecodeCtasPerSm;
+    const int tiles = (max_context_len + kTileTokens - 1) / kTileTokens;
+    int C = 1;
+    while (C * 2 <= kClusterMax && items * C * 2 <= slots && C * 2 <= tiles) C *= 2;
+    if (C < 2) return false;
+    const int chunk = (tiles + C - 1) / C * kTileTokens;
+    if (chunk > kClusterMaxChunk) return false;
+    *C_out = C;
+    *chunk_out = chunk;
+    return true;
+}
 }  // namespace pf
 
 extern "C" {
@@ -585,6 +617,10 @@ int pf_paged_attention_decode_auto_plan(int num_seqs, int num_q_heads, int num_k
     if (sm_count(&sms) != cudaSuccess || sms <= 0) return 0;
     const long long slots = (long long)sms * kDecodeCtasPerSm;
     const long long items = (long long)num_seqs * num_kv_heads;
+    // Few items and short contexts: the cluster split (no workspace) -- C CTAs per item, each
+    // a chunk of at most kClusterMaxChunk tokens, merged through distributed shared memory.
+    int C = 0, chunk = 0;
+    if (cluster_plan(items, sms, max_context_len, &C, &chunk)) return chunk;
     // Enough (sequence, kv head) items, or short contexts: one pass, ordered longest first.
     if (items >= 2 * slots || max_context_len <= 1024) return 0;
     // Otherwise split so that one sequence of the longest length alone spreads over about
@@ -609,6 +645,29 @@ pf_status pf_paged_attention_decode_auto(const void* q, const void* k_cache, con
     size_t need = 0;
     const int P = pf_paged_attention_decode_auto_plan(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                       max_context_len, &need);
+    if (P > 0 && need == 0) {
+        // the cluster split: no workspace
+        const AttnArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                         head_dim, block_size, max_blocks_per_seq, num_blocks, scale};
+        pf_status st = check_attention(a);
+        if (st != PF_OK) return st;
+        if (!aligned(out, 16)) return PF_ERR_INVALID_ARG;
+        int sms = 0, C = 0, chunk = 0;
+        if (sm_count(&sms) != cudaSuccess) return PF_ERR_CUDA;
+        if (!cluster_plan((long long)num_seqs * num_kv_heads, sms, max_context_len, &C, &chunk) || chunk != P)
+            return PF_ERR_CUDA;
+        unsigned* err = nullptr;
+        if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
+        DecodeParams p = make_params(a, err);
+        p.out = out;
+        p.order_mode = ORDER_NATURAL;
+        p.partition_size = chunk;
+        p.cluster_size = C;
+        p.max_context_len = max_context_len;
+        const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, MODE_CLUSTER,
+                                            reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
+    }
     if (P == 0)
         return pf_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
                                          num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,

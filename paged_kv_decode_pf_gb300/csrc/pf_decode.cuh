@@ -391,6 +391,7 @@ template <int D, int G, int NW, int NST, int MODE>
 __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParams p) {
     constexpr bool PART = MODE == MODE_PARTITION;
     constexpr bool APPEND = MODE == MODE_DECODE_APPEND;
+    constexpr bool CLUS = MODE == MODE_CLUSTER;
     using Geo = DecodeGeometry<D, G>;
     constexpr int TT = Geo::TT, ROW = Geo::ROW_BYTES, TILE = Geo::TILE_BYTES;
     constexpr int PSM_PAD = Geo::PSM_PAD;
@@ -404,9 +405,19 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if constexpr (PART) asm volatile("griddepcontrol.launch_dependents;");  // the merge waits for completion
 
+    // cluster split: every CTA announces it has started; the wait before the first write into
+    // another CTA's shared memory (below) ensures that CTA is running
+    if constexpr (CLUS) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
     // ---- which item
     int seq, kvh, part = 0;
-    if (p.order_mode == ORDER_SORTED) {
+    if constexpr (CLUS) {
+        // CTA `part` of its cluster takes chunk `part` of the item's tokens
+        part = int(cluster_ctarank());
+        const int item = blockIdx.x / p.cluster_size;
+        kvh = item % p.num_kv_heads;
+        seq = item / p.num_kv_heads;
+    } else if (p.order_mode == ORDER_SORTED) {
         int* keys = reinterpret_cast<int*>(bars + sorted_keys_offset<NW, NST>() / 8);
         if (!select_sorted_item<NW, PART>(p, keys, &seq, &kvh, &part)) return;
     } else if constexpr (PART) {
@@ -420,6 +431,22 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     }
     const int Hq = p.num_q_heads;
     const int qh0 = kvh * G;
+    // When the item follows from the block index (natural order, cluster split), lane 0 loads the
+    // table entries of this warp's first R tiles alongside the length instead of after it; entries
+    // at or past the length are loaded but never used.
+    const bool spec = CLUS || (!PART && p.order_mode == ORDER_NATURAL);
+    int spec_ent[R];
+    if (spec && (threadIdx.x & 31) == 0) {
+        const int32_t* srow = p.block_tables + size_t(seq) * p.max_blocks_per_seq;
+        const int st0 = CLUS ? part * p.partition_size : 0;
+        const long long cap = min((long long)p.max_blocks_per_seq * p.block_size,
+                                  CLUS ? (long long)st0 + p.partition_size : (long long)INT32_MAX);
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const int tok = (st0 / TT + (threadIdx.x >> 5) + j * NW) * TT;
+            spec_ent[j] = tok < cap ? __ldg(srow + tok / p.block_size) : 0;
+        }
+    }
     const int L = __ldg(p.context_lens + seq);
     bool len_bad = L < 0 || (long long)L > (long long)p.max_blocks_per_seq * p.block_size;
     int t0 = 0, t1 = L;
@@ -428,6 +455,13 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         t0 = part * p.partition_size;
         if (!len_bad && t0 >= L) return;  // empty partition: the merge never reads it
         t1 = min(L, t0 + p.partition_size);
+    }
+    if constexpr (CLUS) {
+        // every CTA of the cluster runs to the cluster barriers: an empty or failed chunk
+        // streams nothing and contributes an empty partial
+        len_bad = len_bad || L > p.max_context_len || (long long)L > (long long)p.partition_size * p.cluster_size;
+        t0 = part * p.partition_size;
+        t1 = len_bad ? t0 : max(t0, min(L, t0 + p.partition_size));
     }
     // Decode with append: the new token of this sequence is its position L-1, and its
     // slot must be that position's slot (or -1: nothing to append).  The slot and the
@@ -448,7 +482,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         return ok ? ((app_slot / p.block_size) * p.num_kv_heads + kvh) * p.block_size + app_slot % p.block_size
                   : -2;
     };
-    if (len_bad) {
+    if (!CLUS && len_bad) {
         if (threadIdx.x == 0) set_error(p.err, ERR_BOUNDS);
         for (int e = threadIdx.x; e < G * D; e += NW * 32) {
             const int h = e / D, d = e % D;
@@ -513,7 +547,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     };
     if (lane == 0) {
 #pragma unroll
-        for (int j = 0; j < R; ++j) ent[j] = j < nk ? __ldg(trow + block_index(tile_token(j))) : 0;
+        for (int j = 0; j < R; ++j) ent[j] = j < nk ? (spec ? spec_ent[j] : __ldg(trow + block_index(tile_token(j)))) : 0;
 #pragma unroll
         for (int k = 0; k < NST; ++k) {
             if (k < nk) {
@@ -607,10 +641,106 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         const size_t slot0 = (size_t(seq) * Hq + qh0) * p.num_partitions + part;
         merge_warps_and_store<D, G, NW>(ml_of, acc_of, failed, p.out + slot0 * D, p.part_m + slot0,
                                         p.part_l + slot0, size_t(p.num_partitions));
+    } else if constexpr (CLUS) {
+        // This chunk's partial -- per element its normalised value, per head its maximum (log2
+        // units) and sum, and a failure flag -- goes straight into the shared memory of the CTA
+        // that finishes the element: CTA r of the cluster merges elements [r SL, (r + 1) SL) of
+        // the G x D output from every chunk's values, after one cluster barrier.
+        constexpr int GD = G * D;
+        const int C = p.cluster_size, SL = GD / C;
+        float* go = reinterpret_cast<float*>(bars + sorted_keys_offset<NW, NST>() / 8);  // [C][SL] values
+        float* gm = go + GD;                                                             // [C][G] maxima
+        float* gl = gm + kClusterMaxSize * G;                                            // [C][G] sums
+        float* gf = gl + kClusterMaxSize * G;                                            // [C] failures
+        const bool bad_here = failed || len_bad;
+        if (len_bad && threadIdx.x == 0 && part == 0) set_error(p.err, ERR_BOUNDS);
+        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster has started
+        for (int e = threadIdx.x; e < GD; e += NW * 32) {
+            const int h = e / D, d = e % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) M = fmaxf(M, ml_of(w)[h]);
+            float wsum = 0.f, o = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    const float f = exp2_approx(ml_of(w)[h] - M);
+                    wsum += f * ml_of(w)[G + h];
+                    o += f * acc_of(w)[h * D + d];
+                }
+            }
+            const float res = bad_here ? NAN : (wsum == 0.f ? 0.f : o / wsum);
+            st_shared_remote(go + part * SL + e % SL, uint32_t(e / SL), res);
+            if (d == 0)
+                for (int r = 0; r < C; ++r) {
+                    st_shared_remote(gm + part * G + h, uint32_t(r), M);
+                    st_shared_remote(gl + part * G + h, uint32_t(r), wsum);
+                }
+        }
+        if (threadIdx.x == 0)
+            for (int r = 0; r < C; ++r) st_shared_remote(gf + part, uint32_t(r), bad_here ? 1.f : 0.f);
+        cluster_sync_all();
+        float* orow = p.out + (size_t(seq) * Hq + qh0) * D;
+        for (int el = threadIdx.x; el < SL; el += NW * 32) {
+            const int e = part * SL + el, h = e / D;
+            float M = -INFINITY;
+            bool bad_any = false;
+            for (int r = 0; r < C; ++r) {
+                M = fmaxf(M, gm[r * G + h]);
+                bad_any = bad_any || gf[r] != 0.f;
+            }
+            float W = 0.f, o = 0.f;
+            if (M != -INFINITY)
+                for (int r = 0; r < C; ++r) {
+                    const float w = gl[r * G + h] * exp2_approx(gm[r * G + h] - M);
+                    W += w;
+                    o += w * go[r * SL + el];
+                }
+            float res = W == 0.f ? 0.f : o / W;  // no token: 0; a NaN input stays NaN
+            if (bad_any) res = NAN;
+            orow[e] = res;
+        }
     } else {
         merge_warps_and_store<D, G, NW>(ml_of, acc_of, failed, p.out + (size_t(seq) * Hq + qh0) * D, nullptr,
                                         nullptr, 1);
     }
+}
+
+// Shared memory past the mbarriers that the cluster split gathers the chunks' partials in:
+// G x D values, and per chunk G maxima, G sums and a flag.
+template <int D, int G>
+constexpr size_t cluster_partial_bytes() { return (size_t(G) * D + size_t(kClusterMaxSize) * (2 * G + 1)) * 4; }
+
+template <int D, int G, int NW, int NST>
+cudaError_t launch_decode_cluster(const DecodeParams& p, cudaStream_t stream) {
+    constexpr size_t smem = decode_smem_bytes<D, G, NW, NST>() + cluster_partial_bytes<D, G>();
+    auto kern = paged_decode_kernel<D, G, NW, NST, MODE_CLUSTER>;
+    static std::atomic<unsigned long long> configured{0};  // one bit per device ordinal
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit == 0 || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const long long grid = (long long)p.num_seqs * p.num_kv_heads * p.cluster_size;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > INT32_MAX) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(NW * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(p.cluster_size);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int D, int G, int NW, int NST, int MODE>

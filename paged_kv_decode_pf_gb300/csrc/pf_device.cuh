@@ -163,6 +163,29 @@ __device__ __forceinline__ float exp2_approx(float x) {
     return y;
 }
 
+// ------------------------------------------------------- thread-block clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster arrives; returns once all have.  Orders the
+// shared-memory writes before the barrier with the reads of other CTAs after it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Stores v into CTA `rank`'s shared memory at the offset of `local` in this CTA's (visible to
+// that CTA after a cluster barrier).
+__device__ __forceinline__ void st_shared_remote(void* local, uint32_t rank, float v) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) {
     if (err != nullptr) atomicOr(err, bits);
 }

@@ -33,7 +33,9 @@ struct DecodeParams {
     int block_size;          // a multiple of 16
     int block_shift;         // log2(block_size) when it is a power of two, else -1
     int max_blocks_per_seq;
-    int partition_size;      // partition pass: tokens per partition (multiple of 16)
+    int partition_size;      // partition pass: tokens per partition; cluster split: tokens per CTA
+                             // (multiples of 16)
+    int cluster_size;        // cluster split: CTAs per (sequence, kv head), 2, 4 or 8
     int num_partitions;      // partition pass: NP
     int max_context_len;     // partition pass: bound every context length must respect
     int order_mode;          // ORDER_NATURAL or ORDER_SORTED (see below)
@@ -49,6 +51,9 @@ struct DecodeParams {
 constexpr int MODE_DECODE = 0;          // single pass over each whole sequence
 constexpr int MODE_PARTITION = 1;       // one context partition per CTA, partials to the workspace
 constexpr int MODE_DECODE_APPEND = 2;   // single pass, after writing each sequence's new token
+constexpr int MODE_CLUSTER = 3;         // a cluster of C CTAs per item, each one chunk of partition_size
+                                        // tokens; the partials merge through distributed shared memory
+constexpr int kClusterMaxSize = 8;      // CTAs per cluster at most (the portable cluster size)
 
 // How CTAs map to work items.
 //  ORDER_NATURAL: CTA b serves (sequence b / Hkv, kv head b % Hkv); partition pass:

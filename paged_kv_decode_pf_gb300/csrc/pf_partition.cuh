@@ -298,6 +298,7 @@ cudaError_t launch_decode_mode(const DecodeParams& p, int mode, cudaStream_t str
             return p.order_mode == ORDER_SORTED ? launch_partition_persistent<D, G, NW, NST>(p, stream)
                                                 : launch_decode_variant<D, G, NW, NST, MODE_PARTITION>(p, stream);
         case MODE_DECODE_APPEND: return launch_decode_variant<D, G, NW, NST, MODE_DECODE_APPEND>(p, stream);
+        case MODE_CLUSTER: return launch_decode_cluster<D, G, NW, NST>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

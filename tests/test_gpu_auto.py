@@ -1,6 +1,7 @@
 """Decode with the library's own choice of decomposition (pf_paged_attention_decode_auto)."""
 import numpy as np
 import pytest
+import torch
 
 from tests.helpers import attn_args, check_close, to_device
 from workloads import make_workload
@@ -12,7 +13,13 @@ def test_plan_single_pass_for_many_items_and_split_for_a_long_few(pf):
     assert pf.decode_auto_plan(256, 32, 8, 128, 8192)[0] == 0          # 2048 items fill the GPU
     P, ws = pf.decode_auto_plan(4, 32, 8, 128, 131072)                   # 32 items, one very long
     assert P >= 256 and P & (P - 1) == 0 and ws == pf.partition_workspace_layout(4, 32, 128, 131072, P)[0]
-    assert pf.decode_auto_plan(4, 32, 8, 128, 900)[0] == 0               # short contexts: one pass
+    assert pf.decode_auto_plan(200, 32, 8, 128, 900)[0] == 0             # many items, short contexts: one pass
+    # few items, contexts a cluster of 8 covers in chunks of <= 1024 tokens: the cluster split
+    # (a chunk size, no workspace)
+    P, ws = pf.decode_auto_plan(4, 32, 8, 128, 900)
+    assert ws == 0 and P == 128                                          # 57 tiles over 8 CTAs
+    P, ws = pf.decode_auto_plan(4, 4, 2, 64, 64)                         # the tiny workload: 4 CTAs of 16 tokens
+    assert ws == 0 and P == 16
 
 
 def test_auto_long_skew_uses_split_and_matches_oracle(pf, oracle_lib, config_workload):
@@ -33,3 +40,73 @@ def test_auto_single_pass_equals_decode(pf):
     a = pf.paged_attention_decode_auto(*attn_args(d), max_context_len=wl.max_context_len).cpu().numpy()
     b = pf.paged_attention_decode(*attn_args(d)).cpu().numpy()
     assert np.array_equal(a, b)
+
+
+def _cluster_plan(pf, wl):
+    P, ws = pf.decode_auto_plan(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.max_context_len)
+    return P, ws
+
+
+@pytest.mark.parametrize("index", [1, 2])
+def test_auto_cluster_split_on_the_small_workloads(pf, oracle_lib, config_workload, index):
+    """The tiny and TinyLlama-shaped workloads have few (sequence, kv head) items: the auto decode
+    runs the cluster split (no workspace) and matches the oracle."""
+    wl = config_workload(index)
+    P, ws = _cluster_plan(pf, wl)
+    assert P > 0 and ws == 0
+    d = to_device(wl)
+    got = pf.paged_attention_decode_auto(*attn_args(d), max_context_len=wl.max_context_len).cpu().numpy()
+    assert pf.get_device_error() == pf.PF_OK
+    ref = oracle_lib.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    check_close(got, ref)
+
+
+# (Hq, Hkv, D, bs, lengths): every group, both head dims, block sizes 16/32/48, empty and
+# one-token sequences, lengths on and off chunk boundaries, chunks past a sequence's end
+CLUSTER_CASES = [
+    (8, 8, 128, 16, [0, 1, 16, 17, 300, 1000]),
+    (16, 8, 128, 32, [5, 64, 65, 999, 1024, 2]),
+    (32, 8, 64, 16, [129, 0, 700, 33]),
+    (32, 4, 64, 48, [1, 2000, 47, 48, 49]),
+    (64, 8, 128, 16, [4000, 12, 3000]),
+    (4, 2, 64, 16, [1, 17, 33, 64]),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs,lengths", CLUSTER_CASES)
+def test_auto_cluster_split_matches_oracle(pf, oracle_lib, Hq, Hkv, D, bs, lengths):
+    wl = make_workload("clu", len(lengths), Hq, Hkv, D, bs, lengths, seed=Hq + D + bs + len(lengths), pool_scale=2)
+    mx = max(wl.max_context_len, 32)
+    P, ws = pf.decode_auto_plan(wl.num_seqs, Hq, Hkv, D, mx)
+    assert P > 0 and ws == 0
+    d = to_device(wl)
+    got = pf.paged_attention_decode_auto(*attn_args(d), max_context_len=mx).cpu().numpy()
+    assert pf.get_device_error() == pf.PF_OK
+    ref = oracle_lib.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    check_close(got, ref)
+    for i, L in enumerate(lengths):
+        if L == 0:
+            assert not got[i].any()
+
+
+def test_auto_cluster_split_bad_length_and_block(pf, oracle_lib):
+    """A length beyond max_context_len and a table entry outside the pool: those sequences' rows
+    are NaN, the others match the oracle, the error word says so; repeated calls are bit-identical."""
+    wl = make_workload("clubad", 4, 16, 4, 128, 16, [300, 200, 500, 150], seed=93, pool_scale=2)
+    mx = wl.max_context_len
+    ref = oracle_lib.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    d = to_device(wl)
+    d["block_tables"][1, 3] = wl.num_blocks + 5
+    d["context_lens"][2] = mx + 1
+    got = pf.paged_attention_decode_auto(*attn_args(d), max_context_len=mx)
+    assert pf.get_device_error() == pf.PF_ERR_DEVICE_BOUNDS
+    g = got.cpu().numpy()
+    assert np.isnan(g[1]).all() and np.isnan(g[2]).all()
+    check_close(g[[0, 3]], ref[[0, 3]])
+    d["block_tables"][1, 3] = int(wl.block_tables[1, 3])
+    d["context_lens"][2] = int(wl.context_lens[2])
+    first = pf.paged_attention_decode_auto(*attn_args(d), max_context_len=mx)
+    outs = [pf.paged_attention_decode_auto(*attn_args(d), max_context_len=mx) for _ in range(50)]
+    assert pf.get_device_error() == pf.PF_OK
+    assert all(torch.equal(o, first) for o in outs)
+    check_close(first.cpu().numpy(), ref)
