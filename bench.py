@@ -58,6 +58,9 @@ def parse_args():
     ap.add_argument("--oracle-seconds", type=float, default=15.0, help="CPU work of the oracle baseline sample")
     ap.add_argument("--seqs", type=int, default=0,
                     help="profiling aid: keep only the first N sequences of the workload (0 = all)")
+    ap.add_argument("--multi-query", type=int, default=0, metavar="Q",
+                    help="profiling aid: time only pf_paged_attention_multi_query with Q new tokens per "
+                         "sequence on the workload's cache and print a short line (0 = the normal bench)")
     ap.add_argument("--decode-variant", default="decode", choices=["decode", "split"],
                     help="headline path: single-pass decode or partition+merge")
     return ap.parse_args()
@@ -516,6 +519,8 @@ def main():
 
     wl = first_sequences(make_config(args.workload), args.seqs)
     runner = Runner(pf, wl, dev, args.decode_variant)
+    if args.multi_query > 0:
+        return profile_multi_query(pf, runner, args)
     flush = None
     if runner.step_bytes() < 2 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -672,6 +677,18 @@ def workload_config(wl, index):
     return {"workload": workload_description(wl, index), "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
             "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
             "total_tokens": int(wl.context_lens.astype(np.int64).sum())}
+
+
+def profile_multi_query(pf, runner, args):
+    """--multi-query Q: the multi-token query alone on the resident cache, for profilers."""
+    mr = MultiQueryRunner(pf, runner, args.multi_query)
+    ms_s, ms_d, per = time_steps(mr, args.steps, max(args.warmup, 3))
+    pf.check_device_error()
+    fl = mr.step_flops()
+    print(json.dumps({"profile": "pf_paged_attention_multi_query", "q_len": args.multi_query,
+                      "rows_per_kv_head": runner.wl.group * args.multi_query, "num_seqs": runner.wl.num_seqs,
+                      "us_mean": round(ms_d * 1e3, 2), "useful_tflops": round(fl / (ms_d * 1e-3) / 1e12, 1),
+                      "algorithmic_bytes": mr.step_bytes()}), flush=True)
 
 
 def first_sequences(wl, n):

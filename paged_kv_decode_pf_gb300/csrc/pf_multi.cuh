@@ -31,10 +31,9 @@ constexpr int kMultiSortMax = 512;
 // The sequence of rank r when the sequences are ordered longest first (ties by index):
 // every CTA ranks the lengths in shared memory, so the hardware's in-order dispatch of
 // the grid starts the longest items first and they do not form the launch's tail.
+// keys: round_up(num_seqs, 4) ints of shared memory (16-byte aligned), s_seq one more.
 template <int NT>
-__device__ __forceinline__ int multi_sorted_seq(const MultiParams& p, int r) {
-    __shared__ __align__(16) int keys[kMultiSortMax];
-    __shared__ int s_seq;
+__device__ __forceinline__ int multi_sorted_seq_into(const MultiParams& p, int r, int* keys, int& s_seq) {
     const int S = p.num_seqs, Sp = (S + 3) & ~3;
     for (int i = threadIdx.x; i < Sp; i += NT) {
         int key = -1;
@@ -58,13 +57,20 @@ __device__ __forceinline__ int multi_sorted_seq(const MultiParams& p, int r) {
     return s_seq;
 }
 
+template <int NT>
+__device__ __forceinline__ int multi_sorted_seq(const MultiParams& p, int r) {
+    __shared__ __align__(16) int keys[kMultiSortMax];
+    __shared__ int s_seq;
+    return multi_sorted_seq_into<NT>(p, r, keys, s_seq);
+}
+
 // Query rows per kv head (g * q_len) above which the prompt-chunk kernel runs, and its
 // upper limit.
 constexpr int kChunkMinRows = 65;
 constexpr int kChunkMaxRows = 1 << 16;
 
-// Launches the prompt-chunk kernel (pf_chunk.cu): one CTA per (sequence, kv head,
-// 128-row tile), scores and P.V on tcgen05 with the query rows as the MMA's M side.
+// Launches the prompt-chunk kernel (pf_chunk.cu): one CTA per (sequence, kv head, 128-row
+// tile), scores and P.V on tcgen05 with the query rows as the MMA's M side.
 // head_dim 64 or 128; the tensor maps view each cache as [NB * Hkv * bs, D] rows in
 // boxes of 16 rows x 64 elements with the 128-byte swizzle.
 cudaError_t launch_chunk(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p, int head_dim,
