@@ -61,8 +61,8 @@ def parse_args():
     ap.add_argument("--multi-query", type=int, default=0, metavar="Q",
                     help="profiling aid: time only pf_paged_attention_multi_query with Q new tokens per "
                          "sequence on the workload's cache and print a short line (0 = the normal bench)")
-    ap.add_argument("--decode-variant", default="decode", choices=["decode", "split"],
-                    help="headline path: single-pass decode or partition+merge")
+    ap.add_argument("--decode-variant", default="decode", choices=["decode", "split", "auto"],
+                    help="headline path: single-pass decode, partition+merge, or the auto decode's own plan")
     return ap.parse_args()
 
 
@@ -641,8 +641,7 @@ def main():
             "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "storage_dtype": "bf16", "data": "synthetic",
             "config": dict(workload_config(wl, args.workload),
-                           step="pf_paged_attention_decode" if not runner_split(args, wl) else
-                           "pf_paged_attention_decode_partition + pf_paged_attention_merge",
+                           step=runner_step(runner),
                            algorithmic_bytes_per_step=step_bytes,
                            l2="inputs larger than L2, no flush" if flush is None else "L2 flushed between steps",
                            parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
@@ -652,7 +651,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": profiled_traffic(CONFIGS[args.workload].name),
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                         else "fallback 6.8 TB/s", "kernel": runner_kernel(args, wl),
+                         else "fallback 6.8 TB/s", "kernel": runner_kernel(runner),
                          "kernel_us_mean": round(ms_dom * 1e3, 2),
                          "kernel_us_p10_p90": [round(float(np.percentile(per, 10)) * 1e3, 2),
                                                round(float(np.percentile(per, 90)) * 1e3, 2)]},
@@ -661,7 +660,7 @@ def main():
                     "note": "every step copies its inputs (q, block tables, lengths) in from pinned host "
                             "memory and its output back, pipelined on two copy streams with double-buffered "
                             "device inputs and outputs; the KV cache stays resident"},
-            "gpu_launches": args.steps * kernels_per_step(args, wl),
+            "gpu_launches": args.steps * runner.kernels_per_step,
             "clocks": clocks,
             "cpu_baseline": cpu,
             "workloads": extras,
@@ -717,16 +716,23 @@ def first_sequences(wl, n):
                                new_k=None if sm is None else wl.new_k[:n], new_v=None if sm is None else wl.new_v[:n])
 
 
-def runner_split(args, wl):
-    return args.decode_variant == "split" or wl.partition_size is not None
+def runner_step(runner):
+    """The timed step's entry points, as the line's config.step names them."""
+    if runner.auto:
+        plan = ("cluster split, chunk %d tokens per CTA" % runner.P if runner.cluster else
+                "partition + merge, P=%d" % runner.P if runner.P else "single pass")
+        return f"pf_paged_attention_decode_auto ({plan})"
+    if runner.split:
+        return "pf_paged_attention_decode_partition + pf_paged_attention_merge"
+    return ("pf_reshape_and_cache + " if runner.append else "") + "pf_paged_attention_decode"
 
 
-def runner_kernel(args, wl):
-    return "paged_decode_kernel (partition pass)" if runner_split(args, wl) else "paged_decode_kernel"
-
-
-def kernels_per_step(args, wl):
-    return (1 if wl.slot_mapping is not None else 0) + (2 if runner_split(args, wl) else 1)
+def runner_kernel(runner):
+    if runner.split or (runner.auto and runner.P and not runner.cluster):
+        return "paged_decode_kernel (partition pass)"
+    if runner.cluster:
+        return "paged_decode_kernel (cluster split)"
+    return "paged_decode_kernel"
 
 
 def reference_arm(args, rank, world):
