@@ -110,3 +110,88 @@ def test_auto_cluster_split_bad_length_and_block(pf, oracle_lib):
     assert pf.get_device_error() == pf.PF_OK
     assert all(torch.equal(o, first) for o in outs)
     check_close(first.cpu().numpy(), ref)
+
+
+def _split_plan(pf, wl, mx):
+    P, ws = pf.decode_auto_plan(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, mx)
+    assert P > 0 and ws > 0, "the workspace split"
+    return P, ws
+
+
+# Batches the auto decode splits over context partitions (S, Hq, Hkv, D, bs, lengths,
+# max_context_len): every group, both head dims, block sizes 16/32/48; empty and one-token
+# rows, lengths on and off 16-token tiles and partition boundaries, one row much longer
+# than the rest, and a batch far shorter than max_context_len.
+SPLIT_CASES = [
+    (20, 32, 8, 128, 16, [0, 1, 15, 16, 17, 1025, 3000, 33, 2048, 0, 7, 900, 1600, 64, 65, 2, 1999, 480, 31, 3000], 3000),
+    (12, 64, 8, 64, 32, [5000, 1, 4096, 33, 0, 2500, 32, 31, 4000, 1200, 64, 4999], 5000),
+    (10, 16, 16, 128, 48, [1100, 47, 48, 49, 0, 2200, 3, 96, 1500, 700], 2200),
+    (2, 8, 4, 128, 16, [20000, 3], 20000),
+    (10, 16, 8, 128, 16, [1, 16, 17, 64, 0, 33, 48, 50, 2, 63], 2000),
+    (12, 8, 8, 64, 16, [0] * 12, 2000),
+]
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,D,bs,lengths,mx", SPLIT_CASES)
+def test_auto_split_matches_oracle(pf, oracle_lib, S, Hq, Hkv, D, bs, lengths, mx):
+    wl = make_workload("autosplit", S, Hq, Hkv, D, bs, lengths, seed=S + Hq + D + bs, pool_scale=2)
+    _split_plan(pf, wl, mx)
+    d = to_device(wl)
+    got = pf.paged_attention_decode_auto(*attn_args(d), max_context_len=mx).cpu().numpy()
+    assert pf.get_device_error() == pf.PF_OK
+    ref = oracle_lib.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    check_close(got, ref)
+    for i, L in enumerate(lengths):
+        if L == 0:
+            assert not got[i].any()
+
+
+def test_auto_split_ignores_workspace_contents_and_repeats(pf, oracle_lib):
+    """The workspace is scratch: NaN-filled or random bytes give the same bits; 30 repeats agree."""
+    wl = make_workload("autows", 12, 32, 8, 128, 16, ("uniform", 1, 6000), seed=97, pool_scale=2)
+    mx = 6000
+    _, ws = _split_plan(pf, wl, mx)
+    d = to_device(wl)
+    w = torch.empty(ws, dtype=torch.uint8, device="cuda")
+    w.view(torch.float32)[: ws // 4].fill_(float("nan"))
+    first = pf.paged_attention_decode_auto(*attn_args(d), max_context_len=mx, workspace=w)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    w.copy_(torch.randint(0, 256, (ws,), dtype=torch.uint8, device="cuda", generator=g))
+    second = pf.paged_attention_decode_auto(*attn_args(d), max_context_len=mx, workspace=w)
+    outs = [pf.paged_attention_decode_auto(*attn_args(d), max_context_len=mx, workspace=w) for _ in range(30)]
+    assert pf.get_device_error() == pf.PF_OK
+    assert torch.equal(first, second) and all(torch.equal(o, first) for o in outs)
+    ref = oracle_lib.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    check_close(first.cpu().numpy(), ref)
+
+
+def test_auto_split_bad_length_and_block(pf, oracle_lib):
+    """A length beyond max_context_len and table entries outside the pool, in a long row and in
+    a short one: those sequences' rows are NaN, the others match the oracle, the error word says so."""
+    lengths = [30000, 500, 200, 40000, 300, 100, 800, 20]
+    wl = make_workload("autobad", 8, 32, 8, 128, 16, lengths, seed=99, pool_scale=2)
+    mx = 40000
+    _split_plan(pf, wl, mx)
+    ref = oracle_lib.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    d = to_device(wl)
+    d["block_tables"][0, 1000] = wl.num_blocks + 5
+    d["block_tables"][4, 2] = -1
+    d["context_lens"][6] = mx + 1
+    got = pf.paged_attention_decode_auto(*attn_args(d), max_context_len=mx)
+    assert pf.get_device_error() == pf.PF_ERR_DEVICE_BOUNDS
+    g = got.cpu().numpy()
+    for i in (0, 4, 6):
+        assert np.isnan(g[i]).all(), i
+    keep = [1, 2, 3, 5, 7]
+    check_close(g[keep], ref[keep])
+
+
+def test_auto_split_equals_decode_within_rounding(pf):
+    wl = make_workload("autoeq", 16, 32, 8, 128, 32, ("loguniform", 16, 16000), seed=101, pool_scale=2)
+    mx = int(wl.max_context_len)
+    _split_plan(pf, wl, mx)
+    d = to_device(wl)
+    a = pf.paged_attention_decode_auto(*attn_args(d), max_context_len=mx)
+    b = pf.paged_attention_decode(*attn_args(d))
+    assert pf.get_device_error() == pf.PF_OK
+    torch.testing.assert_close(a, b, rtol=1e-4, atol=1e-5)
