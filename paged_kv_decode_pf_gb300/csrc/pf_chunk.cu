@@ -109,12 +109,14 @@ struct ChunkSync {
 };
 
 // One producer warp: copies the nt K (or V) tiles of the CTA's sequence into an ns-stage ring
-// (stage s at ring + s * tile_bytes, dim half h at + h * half_bytes).  A tile is eight
-// 16-token boxes; lane l < 8 * HALVES copies dim half l % HALVES of box l / HALVES.  Table
-// entries come 32 boxes (4 tiles) a batch ahead: lane l holds box 32 b + l.  Boxes at or past
-// tmax are not copied.  Before returning it waits for the last fill of every stage, so the
-// CTA never ends with copies in flight.
-template <int HALVES>
+// (stage s at ring + s * tile_bytes).  A tile is eight 16-token boxes.  With BLK false, lane
+// l < 8 * HALVES copies dim half l % HALVES of box l / HALVES to + h * half_bytes + box * 2 KiB
+// (a stage is [dim half][128 rows][128 bytes]); with BLK true (the 3D block map), lane l < 8
+// copies box l whole to + l * HALVES * 2 KiB (a stage is [box][dim half][16 rows][128 bytes]).
+// Table entries come 32 boxes (4 tiles) a batch ahead: lane l holds box 32 b + l.  Boxes at or
+// past tmax are not copied.  Before returning it waits for the last fill of every stage, so
+// the CTA never ends with copies in flight.
+template <int HALVES, bool BLK>
 __device__ __forceinline__ void chunk_produce(const ChunkSync& sy, const MultiParams& p, const CUtensorMap* map,
                                               uint32_t ring, int tile_bytes, int half_bytes, int ns, int fullb,
                                               int emptyb, int seq, int kvh, int tmax, int nt, volatile int* bad,
@@ -132,7 +134,9 @@ __device__ __forceinline__ void chunk_produce(const ChunkSync& sy, const MultiPa
     const uint64_t policy = l2_policy_evict_first();
     int ent_cur = batch(0), ent_nxt = nt > TPB ? batch(1) : 0;
     int issued = 0;
-    const int bi = lane / HALVES, hf = lane % HALVES;
+    constexpr int LPB = BLK ? 1 : HALVES;                                   // lanes per box
+    constexpr uint32_t LANE_BYTES = kTileTokens * 128u * (BLK ? HALVES : 1);  // bytes per lane's copy
+    const int bi = lane / LPB, hf = lane % LPB;
     for (int j = 0; j < nt; ++j) {
         if (j > 0 && j % TPB == 0) {
             ent_cur = ent_nxt;
@@ -140,7 +144,7 @@ __device__ __forceinline__ void chunk_produce(const ChunkSync& sy, const MultiPa
         }
         const int el = __shfl_sync(FULL_MASK, ent_cur, ((j % TPB) * BOXES + bi) & 31);
         const int tok = j * kChTok + bi * kTileTokens;
-        const bool live = lane < BOXES * HALVES && tok < tmax;
+        const bool live = lane < BOXES * LPB && tok < tmax;
         const bool good = live && el >= 0 && (long long)el < p.num_blocks;
         if (live && !good) {
             *bad = 1;
@@ -150,12 +154,16 @@ __device__ __forceinline__ void chunk_produce(const ChunkSync& sy, const MultiPa
         bool ok = true;
         if (lane == 0 && j >= ns) ok = sy.wait(emptyb + s, ((j / ns) - 1) & 1);
         if (!__shfl_sync(FULL_MASK, ok ? 1 : 0, 0)) break;
-        const uint32_t bytes = uint32_t(__popc(__ballot_sync(FULL_MASK, good))) * kTileTokens * 128u;
+        const uint32_t bytes = uint32_t(__popc(__ballot_sync(FULL_MASK, good))) * LANE_BYTES;
         if (lane == 0) mbar_arrive_expect_tx(sy.bar(fullb + s), bytes);
         __syncwarp();  // the byte count is set before any copy can complete
-        if (good)
+        const int row = (el * Hkv + kvh) * bs + block_offset(tok);
+        if (good && BLK)
+            tma_load_3d(ring + uint32_t(s * tile_bytes) + uint32_t(bi) * LANE_BYTES, map, 0, row, 0,
+                        sy.bar(fullb + s), policy);
+        else if (good)
             tma_load_2d(ring + uint32_t(s * tile_bytes + bi * kTileTokens * 128 + hf * half_bytes), map, 64 * hf,
-                        (el * Hkv + kvh) * bs + block_offset(tok), sy.bar(fullb + s), policy);
+                        row, sy.bar(fullb + s), policy);
         ++issued;
     }
     if (lane == 0)
@@ -167,12 +175,16 @@ __device__ __forceinline__ void chunk_produce(const ChunkSync& sy, const MultiPa
 }
 
 // Zero the rows [nvalid, 128) of a V stage (both dim halves): they hold other data or poison,
-// or were not copied, and 0 * V must stay 0.  Called by a whole warp.
-template <int HALVES>
+// or were not copied, and 0 * V must stay 0.  Called by a whole warp.  Row r's 128 bytes of
+// dim half h: + h * half_bytes + r * 128 (BLK false), or + (r / 16) * HALVES * 2 KiB + h * 2 KiB
+// + (r % 16) * 128 (BLK true); the swizzle moves 16-byte chunks only within their row.
+template <int HALVES, bool BLK>
 __device__ __forceinline__ void chunk_zero_v_rows(unsigned char* stage, int half_bytes, int nvalid, int lane) {
     for (int e = lane; e < (kChTok - nvalid) * 8 * HALVES; e += 32) {
         const int r = nvalid + e / (8 * HALVES), c = e % (8 * HALVES);
-        *reinterpret_cast<uint4*>(stage + (c >> 3) * half_bytes + r * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+        const int off = BLK ? (r / kTileTokens) * HALVES * 2048 + (c >> 3) * 2048 + (r % kTileTokens) * 128
+                            : (c >> 3) * half_bytes + r * 128;
+        *reinterpret_cast<uint4*>(stage + off + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -321,6 +333,7 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
                                                                            const MultiParams p) {
     using Lay = ChunkLayout<D>;
     constexpr int NT = kChThreads, TOK = kChTok, NK = Lay::KST, NV = Lay::VST, HALVES = Lay::HALVES;
+    constexpr bool VBLK = kVBlockCopies && HALVES == 2;  // V by whole 16-token blocks (4 KiB copies)
     // mbarriers: K and V rings full / empty; per score buffer: S written, P written, P.V
     // complete (the buffer free again); Q stored; every MMA complete
     enum { KFULL = 0, KEMPTY = NK, VFULL = 2 * NK, VEMPTY = 2 * NK + NV, SFULL = 2 * NK + 2 * NV, PFULL = SFULL + 2,
@@ -378,9 +391,12 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
     if (warp > kChMmaWarp) {
         // ---- producer warps: warp 5 copies K, warp 6 V
         const bool is_v = warp - kChMmaWarp - 1 == 1;
-        chunk_produce<HALVES>(sy, p, is_v ? &tmap_v : &tmap_k, sbase + uint32_t(is_v ? Lay::VRING : Lay::KRING),
-                              Lay::TILE, Lay::HALF, is_v ? NV : NK, is_v ? VFULL : KFULL, is_v ? VEMPTY : KEMPTY, seq,
-                              kvh, tmax, nt, bad, lane);
+        if (is_v)
+            chunk_produce<HALVES, VBLK>(sy, p, &tmap_v, sbase + uint32_t(Lay::VRING), Lay::TILE, Lay::HALF, NV,
+                                        VFULL, VEMPTY, seq, kvh, tmax, nt, bad, lane);
+        else
+            chunk_produce<HALVES, false>(sy, p, &tmap_k, sbase + uint32_t(Lay::KRING), Lay::TILE, Lay::HALF, NK,
+                                         KFULL, KEMPTY, seq, kvh, tmax, nt, bad, lane);
     } else if (warp == kChMmaWarp) {
         // ---- MMA issuer: P(jp) V(jp) when ready, else S(js) (at most two ahead: two score buffers)
         constexpr uint32_t IDESC_S = umma_idesc_bf16(kChRows, TOK, 0, 0);
@@ -436,7 +452,7 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
                 // rows past the sequence, and boxes past the CTA's last token, hold no V row
                 const int vend = min(L, (tmax + kTileTokens - 1) / kTileTokens * kTileTokens);
                 const int nvalid = min(TOK, vend - jp * TOK);
-                if (nvalid < TOK) chunk_zero_v_rows<HALVES>(smem + voff, Lay::HALF, nvalid, lane);
+                if (nvalid < TOK) chunk_zero_v_rows<HALVES, VBLK>(smem + voff, Lay::HALF, nvalid, lane);
                 if (lane == 0) {
                     const uint32_t va = sbase + voff;
                     const uint32_t tp = tmem + ((jp & 1) ? kChTS1 : kChTS0);
@@ -445,7 +461,9 @@ __global__ void __launch_bounds__(kChThreads, 1) paged_chunk_query_kernel(const 
 #pragma unroll
                         for (int kk = 0; kk < TOK / 16; ++kk)  // 16 tokens: 8 TMEM columns of P, 2 KiB of V
                             umma_bf16_tmem_a(tmem + kChTO, tp + uint32_t(64 * part + 8 * kk),
-                                             umma_desc_sw128(va + kk * 2048, Lay::HALF, 1024), IDESC_O,
+                                             VBLK ? umma_desc_sw128(va + kk * 4096, 2048, 1024)
+                                                  : umma_desc_sw128(va + kk * 2048, Lay::HALF, 1024),
+                                             IDESC_O,
                                              (jp | part | kk) != 0);
                     umma_commit(sy.bar(PFREE + (jp & 1)));
                     umma_commit(sy.bar(VEMPTY + jp % NV));

@@ -1392,6 +1392,18 @@ static bool encode_cache_map(CUtensorMap* map, const void* cache, long long rows
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_cache_map_vblocks(CUtensorMap* map, const void* cache, long long rows) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[3] = {64, cuuint64_t(rows), 2};
+    const cuuint64_t strides[2] = {256, 128};  // a row of 128 bf16; the second dim half
+    const cuuint32_t box[3] = {64, cuuint32_t(kTileTokens), 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(cache), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr int kMultiWarps = 4;
 constexpr int kMultiStages = 2;
 
@@ -1533,6 +1545,10 @@ extern "C" pf_status pf_paged_attention_multi_query(const void* q, const void* k
                                            num_blocks, scale, out, &mk, &mv, &p);
     if (st != PF_OK || num_seqs == 0) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const long long cache_rows = num_blocks * num_kv_heads * (long long)block_size;
+    if (p.rows >= kChunkMinRows && head_dim == 128 && kVBlockCopies &&
+        !encode_cache_map_vblocks(&mv, v_cache, cache_rows))
+        return PF_ERR_CUDA;  // the prompt-chunk kernel reads V by whole blocks
     cudaError_t e;
     if (p.rows >= kChunkMinRows)
         e = launch_chunk(mk, mv, p, head_dim, s);  // prompt chunks: query rows on the tcgen05 M side
@@ -1560,6 +1576,9 @@ extern "C" pf_status pf_paged_attention_multi_query_tcgen05(const void* q, const
     if (head_dim != 128) return PF_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PF_OK;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const long long cache_rows = num_blocks * num_kv_heads * (long long)block_size;
+    if (p.rows >= kChunkMinRows && kVBlockCopies && !encode_cache_map_vblocks(&mv, v_cache, cache_rows))
+        return PF_ERR_CUDA;  // the prompt-chunk kernel reads V by whole blocks
     const cudaError_t e = p.rows >= kChunkMinRows ? launch_chunk(mk, mv, p, head_dim, s) : launch_multi_tc(mk, mv, p, s);
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }

@@ -69,10 +69,26 @@ __device__ __forceinline__ int multi_sorted_seq(const MultiParams& p, int r) {
 constexpr int kChunkMinRows = 65;
 constexpr int kChunkMaxRows = 1 << 16;
 
+// At head_dim 128 the prompt-chunk kernel reads V in whole 16-token blocks: one 4 KiB TMA
+// copy of a 3D view of the cache (64 elements, rows, the two dim halves 128 bytes apart),
+// landing as [dim half][16 rows][128 bytes], instead of two 2 KiB copies (1-1.5 % faster
+// there; the 33-64-row tcgen05 kernel, whose V copies go out from more lanes side by side,
+// measured 1.6 % slower with it and keeps the 2 KiB boxes).  K stays in 16-row x 128-byte
+// boxes: its MMA operand needs every dim half's rows at one stride across the tile.
+#ifndef PF_V_BLOCK_COPIES
+#define PF_V_BLOCK_COPIES 1
+#endif
+constexpr bool kVBlockCopies = PF_V_BLOCK_COPIES != 0;
+
+// The cache as a 3D tensor {64 elements, rows = NB * Hkv * bs, 2 dim halves} (D = 128) read in
+// boxes {64, 16, 2} with the 128-byte swizzle.
+bool encode_cache_map_vblocks(CUtensorMap* map, const void* cache, long long rows);
+
 // Launches the prompt-chunk kernel (pf_chunk.cu): one CTA per (sequence, kv head, 128-row
 // tile), scores and P.V on tcgen05 with the query rows as the MMA's M side.
-// head_dim 64 or 128; the tensor maps view each cache as [NB * Hkv * bs, D] rows in
-// boxes of 16 rows x 64 elements with the 128-byte swizzle.
+// head_dim 64 or 128; mk views the K cache as [NB * Hkv * bs, D] rows in boxes of 16 rows x
+// 64 elements with the 128-byte swizzle; mv the V cache the same way, or at D = 128 with
+// kVBlockCopies as encode_cache_map_vblocks does.
 cudaError_t launch_chunk(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& p, int head_dim,
                          cudaStream_t stream);
 

@@ -71,3 +71,21 @@ def test_reference_arm_under_torchrun_two_ranks():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_main_reads_no_deleted_name():
+    """Names that main() deletes (the extras free the headline runner's cache) are not read
+    afterwards on the same path: the default run, extras included, reaches its JSON line."""
+    import ast
+    tree = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    main = next(n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name == "main")
+    deleted = {}
+    for node in ast.walk(main):
+        if isinstance(node, ast.Delete):
+            for t in node.targets:
+                if isinstance(t, ast.Name):
+                    deleted[t.id] = max(deleted.get(t.id, 0), node.lineno)
+    late = [(n.id, n.lineno) for n in ast.walk(main)
+            if isinstance(n, ast.Name) and isinstance(n.ctx, ast.Load) and n.id in deleted
+            and n.lineno > deleted[n.id]]
+    assert not late, late
