@@ -28,12 +28,15 @@ def run_multi(pf, d, q, kernel="auto"):
 
 
 # (Hq, Hkv, D, bs, q_len): g in {1, 4} with q_len in {17, 32, 64, 128} where g * q_len > 64,
-# other groups, head_dim 64, block sizes 16, 32 and 48 (not a power of two)
+# other groups, head_dim 64, block sizes 16, 32 and 48 (not a power of two), and odd numbers
+# of row tiles
 CASES = [
     (32, 8, 128, 16, 17), (32, 8, 128, 16, 32), (32, 8, 128, 16, 64), (32, 8, 128, 16, 128),  # g = 4
     (8, 8, 128, 16, 128), (8, 8, 128, 32, 65), (4, 4, 128, 16, 200),                        # g = 1
     (16, 8, 128, 32, 40), (64, 8, 128, 16, 9), (32, 8, 128, 48, 33),                        # g = 2, 8; bs 48
     (32, 4, 64, 16, 16), (8, 2, 64, 32, 64), (8, 8, 64, 16, 130), (32, 8, 64, 16, 48),      # head_dim 64
+    # an odd number of 128-row tiles (the last cluster pair has an empty second tile)
+    (32, 8, 128, 16, 80), (8, 8, 128, 16, 300), (32, 8, 64, 32, 100),
 ]
 
 
