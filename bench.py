@@ -212,6 +212,10 @@ class Runner:
             self.max_ctx = wl.max_context_len
             self.ws = pf.alloc_workspace(wl.num_seqs, wl.num_q_heads, wl.head_dim, self.max_ctx, self.P, dev)
         self.fused = self.append and not self.split and variant == "fused"
+        self.bf16 = variant == "bf16" and not self.split and not self.append  # the bf16-output single pass
+        if self.bf16:
+            self.out_bf16 = torch.empty((wl.num_seqs, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16,
+                                        device=dev)
         self.kernels_per_step = 1 if self.fused else (1 if self.append else 0) + (
             2 if self.split or (self.auto and self.P and not self.cluster) else 1)
         self.dominant = "partition" if self.split else ("decode_append" if self.fused else "decode")
@@ -244,18 +248,27 @@ class Runner:
                 ev[1].record()
             pf.paged_attention_merge(self.ws, self.cl, self.wl.num_q_heads, self.wl.head_dim, self.P, self.max_ctx,
                                      self.out)
+        elif self.bf16:
+            pf.paged_attention_decode_bf16(self.q, self.kc, self.vc, self.bt, self.cl, self.wl.scale, self.out_bf16)
+            if ev is not None:
+                ev[1].record()
         else:
             pf.paged_attention_decode(self.q, self.kc, self.vc, self.bt, self.cl, self.wl.scale, self.out)
             if ev is not None:
                 ev[1].record()
 
     def step_bytes(self):
-        return self.wl.algorithmic_bytes(with_append=self.append)
+        b = self.wl.algorithmic_bytes(with_append=self.append)
+        if self.bf16:      # the output is written as bf16: 2 bytes per element instead of 4
+            b -= self.wl.num_seqs * self.wl.num_q_heads * self.wl.head_dim * 2
+        return b
 
     def dominant_bytes(self):
         """Algorithmic bytes of the dominant kernel alone."""
         wl = self.wl
         b = wl.algorithmic_bytes(with_append=False)
+        if self.bf16:
+            b -= wl.num_seqs * wl.num_q_heads * wl.head_dim * 2
         if self.split:     # the partition pass reads everything but writes partials, not out
             b -= wl.num_seqs * wl.num_q_heads * wl.head_dim * 4
         return b
@@ -578,8 +591,8 @@ def main():
             del mr
         del runner
         torch.cuda.empty_cache()
-        for idx, variant in [(1, "decode"), (1, "auto"), (2, "decode"), (2, "auto"), (3, "decode"), (3, "fused"), (5, "decode"),
-                             (5, "auto")]:
+        for idx, variant in [(4, "bf16"), (1, "decode"), (1, "auto"), (2, "decode"), (2, "auto"), (3, "decode"),
+                             (3, "fused"), (5, "decode"), (5, "auto")]:
             if idx == args.workload and variant == "decode":
                 continue
             w = make_config(idx)
@@ -590,9 +603,10 @@ def main():
             ms_s, ms_d, _ = time_steps(r, n, 10, fl)
             pf.check_device_error()
             b = r.step_bytes()
-            extras[CONFIGS[idx].name + ("_fused" if r.fused else "_auto" if r.auto else "")] = {
+            extras[CONFIGS[idx].name + ("_fused" if r.fused else "_auto" if r.auto else "_bf16_out" if r.bf16 else "")] = {
                 "description": CONFIGS[idx].description,
                 "step": "append and decode fused in one launch" if r.fused else
+                        "decode with a bf16 output (pf_paged_attention_decode_bf16)" if r.bf16 else
                         (f"decode_auto ({('cluster split, chunk ' + str(r.P) + ' tokens per CTA, one launch') if r.cluster else ('partition + merge, P=' + str(r.P)) if r.P else 'single pass'}, "
                          f"max_context_len {r.max_ctx})") if r.auto else
                         ("append + " if r.append else "") + ("partition + merge" if r.split else "decode"),

@@ -145,6 +145,24 @@ PF_API pf_status pf_paged_attention_decode(const void* q, const void* k_cache, c
                                     float scale, float* out, pf_stream_t stream);
 
 /*
+ * The same single pass with a bf16 output: out is [num_seqs][num_q_heads][head_dim]
+ * bf16 (16-byte aligned, device), each element the fp32 result of
+ * pf_paged_attention_decode rounded once to bf16, to nearest with ties to even --
+ * bit for bit that rounding of the fp32 call's output.  The source pages fix no
+ * output precision (the fp32 entry above is the reading this library takes); this
+ * variant is for callers that feed the attention output straight into a bf16
+ * projection.  Its error against the exact result is the fp32 error plus one bf16
+ * rounding (a relative 2^-9), so it meets |d| <= 2e-3 + 1e-2 |exact| but not the
+ * fp32 entry's 2e-3 absolute bound on outputs of magnitude >= 0.5.  Arguments,
+ * supported shapes and error behaviour are those of pf_paged_attention_decode.
+ */
+PF_API pf_status pf_paged_attention_decode_bf16(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                         int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                         float scale, void* out, pf_stream_t stream);
+
+/*
  * One decode step in one launch: append each sequence's new token, then attend
  * over the cache that includes it (the write and the read sides of "physical KV
  * blocks with logical per-request block tables" and "decode-only block-table

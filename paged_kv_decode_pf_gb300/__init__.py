@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.pf_reshape_and_cache.restype = st
         L.pf_paged_attention_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, f32, P, P]
         L.pf_paged_attention_decode.restype = st
+        L.pf_paged_attention_decode_bf16.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, f32, P, P]
+        L.pf_paged_attention_decode_bf16.restype = st
         L.pf_paged_attention_partition_workspace_layout.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(sz),
                                                                     ctypes.POINTER(sz), ctypes.POINTER(sz)]
         L.pf_paged_attention_partition_workspace_layout.restype = sz
@@ -180,6 +182,24 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                                                block_tables.data_ptr(), context_lens.data_ptr(), S, Hq, Hkv, D, bs,
                                                MB, NB, scale, out.data_ptr(), _stream(q.device)),
                "pf_paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_bf16(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor, scale: Optional[float] = None,
+                                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Single-pass decode attention with a bf16 output [S, Hq, D]: the fp32 result rounded once (to
+    nearest, ties to even)."""
+    S, Hq, Hkv, D, bs, NB, MB = _attn_shapes(q, k_cache, v_cache, block_tables, context_lens)
+    if out is None:
+        out = torch.empty((S, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _cuda(out, "out", _BF16, 3)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        _check(lib().pf_paged_attention_decode_bf16(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                                    block_tables.data_ptr(), context_lens.data_ptr(), S, Hq, Hkv, D,
+                                                    bs, MB, NB, scale, out.data_ptr(), _stream(q.device)),
+               "pf_paged_attention_decode_bf16")
     return out
 
 

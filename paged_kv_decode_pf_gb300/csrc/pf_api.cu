@@ -433,6 +433,27 @@ pf_status pf_paged_attention_decode(const void* q, const void* k_cache, const vo
     return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
 }
 
+pf_status pf_paged_attention_decode_bf16(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                         int max_blocks_per_seq, int64_t num_blocks, float scale, void* out,
+                                         pf_stream_t stream) {
+    const AttnArgs a{q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, max_blocks_per_seq, num_blocks, scale};
+    pf_status st = check_attention(a);
+    if (st != PF_OK) return st;
+    if (num_seqs == 0) return PF_OK;
+    if (!aligned(out, 16)) return PF_ERR_INVALID_ARG;
+    unsigned* err = nullptr;
+    if (error_word(&err) != cudaSuccess) return PF_ERR_CUDA;
+    DecodeParams p = make_params(a, err);
+    p.out_bf16 = static_cast<uint16_t*>(out);
+    p.order_mode = decode_order(num_seqs, num_kv_heads);
+    const cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, MODE_DECODE,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PF_OK : PF_ERR_CUDA;
+}
+
 pf_status pf_paged_attention_decode_append(const void* q, const void* k_new, const void* v_new,
                                            const int64_t* slot_mapping, void* k_cache, void* v_cache,
                                            const int32_t* block_tables, const int32_t* context_lens, int num_seqs,

@@ -357,12 +357,21 @@ struct WarpAttention {
     }
 };
 
+// fp32 -> bf16 bits, rounded to nearest with ties to even (a NaN stays a NaN).
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
+    return r;
+}
+
 // Merge the NW warps' stashes of one item and write it: element e = h * D + d of the
 // group; ml(w) / accs(w) locate warp w's (m, l) pairs and [G][D] accumulator.  Writes
-// out_rows[h * D + d] (normalised), and for a partition its natural-log max and sum.
+// out_rows[h * D + d] (normalised) -- or, when out_bf16 is set, its bf16 rounding to
+// out_bf16[h * D + d] -- and for a partition its natural-log max and sum.
 template <int D, int G, int NW, typename MlFn, typename AccFn>
 __device__ __forceinline__ void merge_warps_and_store(MlFn ml, AccFn accs, bool failed, float* out_rows,
-                                                      float* part_m, float* part_l, size_t part_stride) {
+                                                      float* part_m, float* part_l, size_t part_stride,
+                                                      uint16_t* out_bf16 = nullptr) {
     for (int e = threadIdx.x; e < G * D; e += NW * 32) {
         const int h = e / D, d = e % D;
         float M = -INFINITY;
@@ -379,7 +388,8 @@ __device__ __forceinline__ void merge_warps_and_store(MlFn ml, AccFn accs, bool 
         }
         float res = wsum == 0.f ? 0.f : o / wsum;  // no token: 0; a NaN input stays NaN
         if (failed) res = NAN;
-        out_rows[h * part_stride * D + d] = res;
+        if (out_bf16 != nullptr) out_bf16[h * part_stride * D + d] = f32_to_bf16_rn(res);
+        else out_rows[h * part_stride * D + d] = res;
         if (part_m != nullptr && d == 0) {
             part_m[h * part_stride] = failed ? NAN : M * 0.6931471805599453f;
             part_l[h * part_stride] = failed ? NAN : wsum;
@@ -701,8 +711,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
             orow[e] = res;
         }
     } else {
-        merge_warps_and_store<D, G, NW>(ml_of, acc_of, failed, p.out + (size_t(seq) * Hq + qh0) * D, nullptr,
-                                        nullptr, 1);
+        const size_t row0 = (size_t(seq) * Hq + qh0) * D;
+        if (p.out_bf16 != nullptr)
+            merge_warps_and_store<D, G, NW>(ml_of, acc_of, failed, nullptr, nullptr, nullptr, 1, p.out_bf16 + row0);
+        else
+            merge_warps_and_store<D, G, NW>(ml_of, acc_of, failed, p.out + row0, nullptr, nullptr, 1);
     }
 }
 

@@ -23,6 +23,8 @@ struct DecodeParams {
     float* out;        // decode: out [S, Hq, D]; partition pass: tmp_out [S, Hq, NP, D]
     float* part_m;     // partition pass only: tmp_m [S, Hq, NP] (natural-log units)
     float* part_l;     // partition pass only: tmp_l [S, Hq, NP]
+    uint16_t* out_bf16;  // single pass only: when set, out [S, Hq, D] in bf16 (each fp32 result rounded
+                         // to nearest, ties to even) instead of `out`
     unsigned* err;     // device error word
     long long num_blocks;
     unsigned long long wait_limit_ns;

@@ -63,23 +63,35 @@ def test_workspace_layout_arithmetic(lib):
         assert pf.partition_workspace_layout(*bad)[0] == 0
 
 
-def _decode(lib, **kw):
+def _decode(lib, fn=None, **kw):
     a = dict(q=0x10000, kc=0x20000, vc=0x30000, bt=0x40000, cl=0x50000, S=2, Hq=8, Hkv=2, D=128, bs=16, MB=4,
              NB=64, scale=0.125, out=0x60000)
     a.update(kw)
-    return lib.pf_paged_attention_decode(a["q"], a["kc"], a["vc"], a["bt"], a["cl"], a["S"], a["Hq"], a["Hkv"],
-                                         a["D"], a["bs"], a["MB"], a["NB"], a["scale"], a["out"], None)
+    fn = lib.pf_paged_attention_decode if fn is None else fn
+    return fn(a["q"], a["kc"], a["vc"], a["bt"], a["cl"], a["S"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["MB"],
+              a["NB"], a["scale"], a["out"], None)
 
 
-@pytest.mark.parametrize("change,want", [
+DECODE_CHECKS = [
     (dict(S=-1), 1), (dict(Hq=0), 1), (dict(Hkv=0), 1), (dict(Hq=6, Hkv=4), 1), (dict(D=0), 1),
     (dict(bs=0), 1), (dict(MB=0), 1), (dict(NB=0), 1), (dict(NB=2 ** 31), 1), (dict(scale=float("inf")), 1),
     (dict(q=None), 1), (dict(q=0x10002), 1), (dict(bt=0x40002), 1), (dict(out=0x60004), 1),
     (dict(D=96), 2), (dict(D=256), 2), (dict(bs=8), 2), (dict(bs=24), 2), (dict(Hq=32, Hkv=2), 2),
     (dict(Hq=6, Hkv=2), 2),
-])
+]
+
+
+@pytest.mark.parametrize("change,want", DECODE_CHECKS)
 def test_decode_host_validation(lib, change, want):
     assert _decode(lib, **change) == want
+
+
+@pytest.mark.parametrize("change,want", DECODE_CHECKS + [(dict(out=None), 1), (dict(out=0x60002), 1)])
+def test_decode_bf16_host_validation(lib, change, want):
+    """The bf16-output entry checks its arguments as the fp32 one does (its output 16-byte aligned)."""
+    assert _decode(lib, fn=lib.pf_paged_attention_decode_bf16, **change) == want
+    assert _decode(lib, fn=lib.pf_paged_attention_decode_bf16, S=0, q=None, kc=None, vc=None, bt=None, cl=None,
+                   out=None) == 0
 
 
 def test_zero_sequences_is_a_no_op(lib):
